@@ -1,0 +1,200 @@
+/*
+ * CPU fp64 oracle for ubatch-aligned paged attention (UA-PagedAttention).
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the plain, slow, obviously correct
+ * statement of what the GPU path computes.  Only the test suite, the smoke
+ * check and the CPU-baseline leg of the benchmark may load it.  It shares no
+ * code, header, table or helper with the CUDA library; the product path never
+ * calls it.
+ *
+ * Source of the method: "面向多并发长上下文的 llama.cpp 分页式 KV Cache 与计算加速优化"
+ * (gitlink IFwnjPgFSU/mxzntdncglxtsjysx), section 作品简介: the KV cache keeps a
+ * page mapping and a true length per sequence; at graph build the page table
+ * and the true KV length are expanded per ubatch token, in token order, by the
+ * sequence each token belongs to; the backend operator then reads only the
+ * valid pages of each query's own sequence.  The result is ordinary causal,
+ * sequence-restricted softmax attention -- paging only changes which cells are
+ * touched -- so the oracle is that definition written out.
+ *
+ * Readings taken where the page is silent (each is listed in the design notes):
+ *   - tok_kv_len[t] is the number of keys token t may see (its position + 1:
+ *     the token's own K/V row is appended before attention);
+ *   - query head h reads KV head h / (Hq / Hkv) (contiguous GQA grouping);
+ *   - softmax is base e of scale * q.k, with max subtraction;
+ *   - tok_kv_len[t] == 0 gives an all-zero output row;
+ *   - slot_mapping[t] < 0 means "do not write" (padding token);
+ *   - pool layout is [num_pages][Hkv][P][d], binary16 values.
+ *
+ * Parity pins (tests, not this file): brute-force unpaged attention from the
+ * contiguous K/V before paging, torch SDPA in fp64 for one sequence, a
+ * hand-derived closed-form fixture, and invariants (page permutation, NaN in
+ * free cells, constant V, kv_len = 1, q = 0, shared prefix pages).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* IEEE 754 binary16 -> double, exact.  sign | 5-bit exponent (bias 15) | 10-bit fraction. */
+double ref_f16_to_f64(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int m = h & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -24);               /* subnormal: m * 2^-14 * 2^-10 */
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + m), e - 25);   /* (1 + m/1024) * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+/*
+ * Per-token expansion of the page table and true KV length (作品简介: "将页表和
+ * 真实 KV 长度按 token 顺序展开").  For ubatch token t of sequence s at position p:
+ *   tok_page_table[t][:] = seq_page_table[s][:]
+ *   tok_kv_len[t]        = p + 1
+ *   slot_mapping[t]      = page * P + p % P, page = seq_page_table[s][p / P]
+ * tok_seq[t] < 0 marks a padding token: row of -1, kv_len 0, slot -1.
+ * A position whose page is not allocated (-1) gets slot -1.
+ * Returns 0, or -1 if a sequence index or position is out of range.
+ */
+int ref_expand_ubatch(const int32_t *seq_page_table, int n_seq, int max_pages,
+                      const int32_t *tok_seq, const int32_t *tok_pos, int T, int P,
+                      int32_t *tok_page_table, int32_t *tok_kv_len, int64_t *slot_mapping)
+{
+    for (int t = 0; t < T; ++t) {
+        int s = tok_seq[t];
+        int32_t *row = tok_page_table + (size_t)t * max_pages;
+        if (s < 0) {
+            for (int i = 0; i < max_pages; ++i) row[i] = -1;
+            tok_kv_len[t] = 0;
+            slot_mapping[t] = -1;
+            continue;
+        }
+        if (s >= n_seq) return -1;
+        int p = tok_pos[t];
+        if (p < 0 || p / P >= max_pages) return -1;
+        const int32_t *srow = seq_page_table + (size_t)s * max_pages;
+        for (int i = 0; i < max_pages; ++i) row[i] = srow[i];
+        tok_kv_len[t] = p + 1;
+        int page = srow[p / P];
+        slot_mapping[t] = page < 0 ? -1 : (int64_t)page * P + (p % P);
+    }
+    return 0;
+}
+
+/*
+ * reshape-and-cache (CacheFlow, 核心架构 3): write each token's new K and V rows
+ * into its slot.  slot = page * P + offset; the row lands at
+ * pages[page][h][offset][0:d].  Bit copy; slots < 0 are skipped.
+ * Returns 0, or -1 if a slot is beyond the pool.
+ */
+int ref_kv_append(const uint16_t *k, const uint16_t *v, const int64_t *slot_mapping, int T,
+                  uint16_t *k_pages, uint16_t *v_pages, int num_pages, int Hkv, int P, int d)
+{
+    for (int t = 0; t < T; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;
+        if (slot >= (int64_t)num_pages * P) return -1;
+        int64_t page = slot / P, off = slot % P;
+        for (int h = 0; h < Hkv; ++h) {
+            size_t dst = (((size_t)page * Hkv + h) * P + off) * d;
+            size_t src = ((size_t)t * Hkv + h) * d;
+            memcpy(k_pages + dst, k + src, (size_t)d * sizeof(uint16_t));
+            memcpy(v_pages + dst, v + src, (size_t)d * sizeof(uint16_t));
+        }
+    }
+    return 0;
+}
+
+/*
+ * Paged attention, by definition.  For each selected token t and query head h,
+ * with L = tok_kv_len[t] and g = h / (Hq / Hkv):
+ *   K_t[j] = k_pages[tok_page_table[t][j / P]][g][j % P][:]   (j < L), same for V
+ *   s_j    = scale * sum_i q[t][h][i] * K_t[j][i]
+ *   out[t][h][:] = sum_j softmax(s)_j * V_t[j][:]
+ * all in double.  The K/V of the token are first gathered into contiguous
+ * buffers, then the softmax is computed -- no blocking, no online rescaling.
+ *
+ * tokens == NULL selects all T tokens (out is [T][Hq][d]); otherwise the n_tok
+ * listed token indices are computed and out is [n_tok][Hq][d].
+ * Returns 0, or -1 on a page id outside [0, num_pages) or L beyond the row.
+ */
+int ref_paged_attention(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
+                        const int32_t *tok_page_table, int max_pages, const int32_t *tok_kv_len,
+                        int T, int Hq, int Hkv, int P, int d, int num_pages, double scale,
+                        const int32_t *tokens, int n_tok, double *out)
+{
+    int G = Hq / Hkv;
+    int n = tokens ? n_tok : T;
+    int bad = 0;
+    long long pairs = (long long)n * Hq;
+#pragma omp parallel for schedule(dynamic, 1) reduction(|: bad)
+    for (long long pi = 0; pi < pairs; ++pi) {
+        int ti = (int)(pi / Hq), h = (int)(pi % Hq);
+        int t = tokens ? tokens[ti] : ti;
+        int g = h / G;
+        int L = tok_kv_len[t];
+        double *o = out + ((size_t)ti * Hq + h) * d;
+        for (int i = 0; i < d; ++i) o[i] = 0.0;
+        if (L <= 0) continue;
+        if (L > max_pages * P) { bad = 1; continue; }
+        double *Kt = (double *)malloc(sizeof(double) * (size_t)L * d);
+        double *Vt = (double *)malloc(sizeof(double) * (size_t)L * d);
+        double *s = (double *)malloc(sizeof(double) * (size_t)L);
+        const int32_t *row = tok_page_table + (size_t)t * max_pages;
+        int ok = 1;
+        /* gather this token's keys and values through its page-table row */
+        for (int j = 0; j < L && ok; ++j) {
+            int page = row[j / P];
+            if (page < 0 || page >= num_pages) { ok = 0; break; }
+            size_t base = (((size_t)page * Hkv + g) * P + (j % P)) * d;
+            for (int i = 0; i < d; ++i) {
+                Kt[(size_t)j * d + i] = ref_f16_to_f64(k_pages[base + i]);
+                Vt[(size_t)j * d + i] = ref_f16_to_f64(v_pages[base + i]);
+            }
+        }
+        if (ok) {
+            const uint16_t *qh = q + ((size_t)t * Hq + h) * d;
+            double m = -INFINITY;
+            for (int j = 0; j < L; ++j) {
+                double acc = 0.0;
+                for (int i = 0; i < d; ++i) acc += ref_f16_to_f64(qh[i]) * Kt[(size_t)j * d + i];
+                s[j] = scale * acc;
+                if (s[j] > m) m = s[j];
+            }
+            double Z = 0.0;
+            for (int j = 0; j < L; ++j) { s[j] = exp(s[j] - m); Z += s[j]; }
+            for (int j = 0; j < L; ++j) {
+                double w = s[j] / Z;
+                for (int i = 0; i < d; ++i) o[i] += w * Vt[(size_t)j * d + i];
+            }
+        } else {
+            bad = 1;
+        }
+        free(Kt); free(Vt); free(s);
+    }
+    return bad ? -1 : 0;
+}
+
+/* Number of threads the OpenMP runtime will use (reported beside CPU timings). */
+int ref_num_threads(void)
+{
+    int n = 1;
+#pragma omp parallel
+    {
+#pragma omp single
+        {
+#ifdef _OPENMP
+            n = omp_get_num_threads();
+#endif
+        }
+    }
+    return n;
+}
