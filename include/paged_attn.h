@@ -1,0 +1,222 @@
+/*
+ * paged_attn.h -- C ABI of the GB300 (sm_103a) ubatch-aligned paged attention
+ * library (libpagedattn.so).
+ *
+ * The method: "面向多并发长上下文的 llama.cpp 分页式 KV Cache 与计算加速优化"
+ * (gitlink IFwnjPgFSU/mxzntdncglxtsjysx), section 作品简介.  The KV cache keeps,
+ * per sequence, a page mapping and a true KV length; at graph build both are
+ * expanded per ubatch token in token order; the attention operator then reads,
+ * for each query, only the valid pages of that query's own sequence -- never
+ * the free cells or padding of a unified span.  The companion write of new K/V
+ * rows into their pages is the "reshape-and-cache" kernel of the CacheFlow page
+ * (section 核心架构 3).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - f16 data are IEEE binary16 values passed as uint16_t bit patterns.
+ *  - KV pool: k_pages and v_pages, each [num_pages][Hkv][P][d], contiguous.
+ *    Sequence position p lives in page tok_page_table[t][p / P] at in-page
+ *    offset p % P.  One (page, KV head) tile is contiguous.
+ *  - q and out: [T][Hq][d]; new K/V rows k and v: [T][Hkv][d]; contiguous.
+ *  - Query head h reads KV head h / (Hq / Hkv) (contiguous GQA grouping).
+ *  - tok_kv_len[t] is the number of keys token t attends to: keys 0 ..
+ *    tok_kv_len[t]-1 of its sequence (causal prefill: position + 1).  A value of
+ *    0 gives an all-zero output row.
+ *  - tok_page_table rows are padded with -1 past the sequence's pages.  Tokens
+ *    whose rows are byte-identical may share tensor-core tiles; pad rows
+ *    canonically (the same way for every token of a sequence).
+ *  - Supported shapes: d in {64, 128}; P in {16, 32, 64, 128}; Hq % Hkv == 0
+ *    with Hq / Hkv in {1, 2, 4, 8}; T >= 0.  Others return PA_EUNSUPPORTED.
+ *  - All pointers except `stream` are DEVICE pointers unless stated.  Device
+ *    buffers must be 16-byte aligned.  The caller owns every buffer; the
+ *    library allocates no device memory.  Calls are asynchronous on `stream`
+ *    (a cudaStream_t; NULL = legacy default stream) and never synchronise,
+ *    except paged_attn_read_error.
+ *  - Errors: host-side argument checks return a negative status before any
+ *    launch.  Device-side problems (a page id outside [0, num_pages), a
+ *    kv_len beyond the row's capacity, a bounded wait that timed out) never
+ *    trap: the kernel skips the bad access, records a PA_ERR_* bit in the
+ *    workspace error word, and paged_attn_read_error returns it.
+ */
+#ifndef PAGED_ATTN_H
+#define PAGED_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define PA_OK 0
+#define PA_EINVAL (-1)        /* null pointer, negative size, inconsistent shapes */
+#define PA_EUNSUPPORTED (-2)  /* shape outside the supported set */
+#define PA_EWORKSPACE (-3)    /* workspace missing or smaller than required */
+#define PA_ELAUNCH (-4)       /* a CUDA launch or runtime call failed */
+#define PA_EDEVICE (-5)       /* the device error word is non-zero (see PA_ERR_*) */
+#define PA_EALIGN (-6)        /* a device pointer is not 16-byte aligned */
+
+/* Bits of the device error word. */
+#define PA_ERR_PAGE_RANGE 0x1   /* a page id needed by some token is outside [0, num_pages) */
+#define PA_ERR_KV_RANGE 0x2     /* tok_kv_len[t] < 0 or > max_pages * P */
+#define PA_ERR_SLOT_RANGE 0x4   /* slot_mapping[t] >= num_pages * P */
+#define PA_ERR_TIMEOUT 0x8      /* a bounded device-side wait gave up */
+#define PA_ERR_SEQ_RANGE 0x10   /* expansion: tok_seq[t] >= n_seq or position beyond the row */
+
+/* Human-readable text of a status code (static storage). */
+const char *paged_attn_strerror(int status);
+
+/* ABI version of this library (major * 100 + minor). */
+int paged_attn_version(void);
+
+/*
+ * Per-token expansion of the page table and the true KV length (page section
+ * 作品简介: "依据 ubatch 中各 token 的序列归属将页表和真实 KV 长度按 token 顺序展开").
+ *
+ *   seq_page_table [n_seq][max_pages] int32  per-sequence physical page ids, -1 padded
+ *   tok_seq [T] int32     sequence of each ubatch token; < 0 marks a padding token
+ *   tok_pos [T] int32     position of the token in its sequence
+ *   tok_page_table [T][max_pages] int32 (out)  copy of the token's sequence row
+ *   tok_kv_len [T] int32 (out)                 tok_pos + 1 (0 for padding)
+ *   slot_mapping [T] int64 (out)               page * P + tok_pos % P, with
+ *       page = row[tok_pos / P]; -1 for padding or an unallocated page
+ *   err (device, optional, may be NULL): PA_ERR_SEQ_RANGE is OR-ed in when a
+ *       token names a sequence >= n_seq or a position beyond its row; such a
+ *       token is expanded as padding.
+ * One launch.  Returns PA_OK or a negative status.
+ */
+int paged_expand_ubatch(const int32_t *seq_page_table, int n_seq, int max_pages,
+                        const int32_t *tok_seq, const int32_t *tok_pos, int T, int P,
+                        int32_t *tok_page_table, int32_t *tok_kv_len, int64_t *slot_mapping,
+                        int *err, void *stream);
+
+/*
+ * reshape-and-cache (CacheFlow page, section 核心架构 3): write the new K and V
+ * rows of each ubatch token into their slots.
+ *
+ *   k, v [T][Hkv][d] binary16      new rows
+ *   slot_mapping [T] int64          slot = page * P + offset; < 0 = skip token
+ *   k_pages, v_pages [num_pages][Hkv][P][d] binary16 (in/out)
+ *   err (device, optional): PA_ERR_SLOT_RANGE is OR-ed in for a slot beyond the
+ *       pool; that token is skipped.
+ * Bit copy: the pool after the call differs from before only in the written
+ * rows.  One launch.
+ */
+int paged_kv_append(const uint16_t *k, const uint16_t *v, const int64_t *slot_mapping, int T,
+                    uint16_t *k_pages, uint16_t *v_pages, int num_pages, int Hkv, int P, int d,
+                    int *err, void *stream);
+
+/*
+ * Bytes of device workspace that paged_attn_plan / _prefill / _decode /
+ * _forward need for a ubatch of T tokens (current device's SM count is used).
+ * Returns 0 for unsupported shapes.
+ */
+size_t paged_attn_workspace_size(int T, int Hq, int Hkv, int d);
+
+/*
+ * Plan a ubatch (device-side, no host round trip, graph-capturable).  Finds
+ * runs of consecutive tokens whose page-table rows are byte-identical; runs of
+ * at least the prefill threshold (paged_attn_set_prefill_min_run) become
+ * tensor-core tiles of up to 128 tokens; the remaining tokens become decode
+ * work, split along the KV axis over all SMs.  Also clears the workspace error
+ * word.  The plan stays valid for any number of later _prefill / _decode /
+ * _run calls with the same tok_page_table / tok_kv_len contents (for example
+ * once per layer).
+ */
+int paged_attn_plan(const int32_t *tok_page_table, int max_pages, const int32_t *tok_kv_len,
+                    int T, int Hq, int Hkv, int P, int d,
+                    void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Prefill part of the attention: every planned tile computes
+ *   out[t][h] = softmax_j(scale * q[t][h] . K_t[j]) V_t[j],  j < tok_kv_len[t],
+ * with K_t/V_t read through the tile's page-table row, on tcgen05 tensor cores
+ * (f16 inputs, f32 accumulation, f16 output).  Writes only the rows of tile
+ * tokens.  Requires a preceding paged_attn_plan on the same workspace.
+ */
+int paged_attn_prefill(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
+                       const int32_t *tok_page_table, int max_pages, const int32_t *tok_kv_len,
+                       int T, int Hq, int Hkv, int P, int d, int num_pages, float scale,
+                       uint16_t *out, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Decode part: split-KV attention for the planned decode tokens (GQA-grouped,
+ * each KV block read once per KV head), then the log-sum-exp reduce of the
+ * splits (CacheFlow page, section 核心架构 3: partition + reduce for long
+ * contexts).  Writes only the rows of decode tokens.  Requires a preceding
+ * paged_attn_plan on the same workspace.
+ */
+int paged_attn_decode(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
+                      const int32_t *tok_page_table, int max_pages, const int32_t *tok_kv_len,
+                      int T, int Hq, int Hkv, int P, int d, int num_pages, float scale,
+                      uint16_t *out, void *workspace, size_t workspace_bytes, void *stream);
+
+/* paged_attn_prefill followed by paged_attn_decode (a planned ubatch). */
+int paged_attn_run(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
+                   const int32_t *tok_page_table, int max_pages, const int32_t *tok_kv_len,
+                   int T, int Hq, int Hkv, int P, int d, int num_pages, float scale,
+                   uint16_t *out, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * The whole attention for one ubatch: paged_attn_plan then paged_attn_run.
+ * out[t][h] for every token t and query head h.  workspace_bytes must be at
+ * least paged_attn_workspace_size(T, Hq, Hkv, d).
+ */
+int paged_attn_forward(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
+                       const int32_t *tok_page_table, int max_pages, const int32_t *tok_kv_len,
+                       int T, int Hq, int Hkv, int P, int d, int num_pages, float scale,
+                       uint16_t *out, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Check the tables without trapping: every page id a token needs
+ * (row[0 .. ceil(kv_len/P)-1]) must lie in [0, num_pages) and 0 <= kv_len <=
+ * max_pages * P.  OR-s PA_ERR_PAGE_RANGE / PA_ERR_KV_RANGE into *err (device).
+ */
+int paged_attn_validate(const int32_t *tok_page_table, int max_pages, const int32_t *tok_kv_len,
+                        int T, int P, int num_pages, int *err, void *stream);
+
+/*
+ * Synchronise `stream` and copy the workspace error word to *err_host (host
+ * pointer).  Returns PA_OK if it is zero, PA_EDEVICE otherwise.
+ */
+int paged_attn_read_error(const void *workspace, int *err_host, void *stream);
+
+/*
+ * Tuning knob: the shortest run of consecutive same-row tokens that is sent
+ * to the tensor-core prefill path (default 16; 1 sends every token there,
+ * a huge value sends every token to the decode path).  Process-wide; affects
+ * plans made after the call.  Returns the previous value.
+ */
+int paged_attn_set_prefill_min_run(int min_run);
+
+/*
+ * Host-side page pool (the per-sequence page mapping of 作品简介; CacheFlow
+ * section 核心架构 2: fixed-size blocks with a block table, blocks shared by
+ * reference count).  Pure host code; no CUDA call.  Page ids are handed out
+ * lowest-first from a free list; a page returns to the free list when its
+ * reference count drops to zero.
+ */
+typedef struct pa_page_pool pa_page_pool;
+
+/* New pool of num_pages pages, all free.  NULL on bad size or allocation failure. */
+pa_page_pool *pa_pool_create(int num_pages);
+void pa_pool_destroy(pa_page_pool *pool);
+/* Number of free pages. */
+int pa_pool_num_free(const pa_page_pool *pool);
+/* Take n free pages (refcount 1) into out_pages (host array of n).  Returns n,
+ * or PA_EINVAL / -7 (PA_ENOSPACE) without taking any when fewer than n are free. */
+#define PA_ENOSPACE (-7)
+int pa_pool_alloc(pa_page_pool *pool, int n, int32_t *out_pages);
+/* Add one reference to each of the n pages (sharing, e.g. a common prefix). */
+int pa_pool_share(pa_page_pool *pool, const int32_t *pages, int n);
+/* Drop one reference from each of the n pages; pages reaching zero are freed. */
+int pa_pool_release(pa_page_pool *pool, const int32_t *pages, int n);
+/* Reference count of one page (0 = free), or PA_EINVAL. */
+int pa_pool_refcount(const pa_page_pool *pool, int32_t page);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGED_ATTN_H */

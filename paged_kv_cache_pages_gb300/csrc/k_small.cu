@@ -1,0 +1,240 @@
+// Small kernels of the paged-attention path (sm_103a):
+//   k_expand   per-token expansion of the page table and true KV length
+//              (UA-PagedAttention page, section 作品简介)
+//   k_append   reshape-and-cache: scatter new K/V rows into their page slots
+//              (CacheFlow page, section 核心架构 3)
+//   k_validate table check without trapping
+//   k_plan     one-CTA device planner: same-row runs -> tensor-core tiles,
+//              short runs -> split-KV decode work
+#include "kernels.cuh"
+
+namespace pa {
+
+// ---------------------------------------------------------------------------
+// Expansion.  One warp per token: the row copy is 128-byte coalesced.
+// ---------------------------------------------------------------------------
+__global__ void k_expand(const int32_t *__restrict__ seq_pt, int n_seq, int max_pages,
+                         const int32_t *__restrict__ tok_seq, const int32_t *__restrict__ tok_pos,
+                         int T, int P, int32_t *__restrict__ tok_pt, int32_t *__restrict__ tok_kv,
+                         int64_t *__restrict__ slot, int *err) {
+  int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  int lane = threadIdx.x & 31;
+  int nwarps = (gridDim.x * blockDim.x) >> 5;
+  for (int t = warp; t < T; t += nwarps) {
+    int s = tok_seq[t];
+    int p = tok_pos[t];
+    bool bad = s >= n_seq || (s >= 0 && (p < 0 || p / P >= max_pages));
+    if (bad && lane == 0 && err) atomicOr(err, PA_ERR_SEQ_RANGE);
+    int32_t *row = tok_pt + (size_t)t * max_pages;
+    if (s < 0 || bad) {
+      for (int i = lane; i < max_pages; i += 32) row[i] = -1;
+      if (lane == 0) { tok_kv[t] = 0; slot[t] = -1; }
+      continue;
+    }
+    const int32_t *srow = seq_pt + (size_t)s * max_pages;
+    for (int i = lane; i < max_pages; i += 32) row[i] = srow[i];
+    if (lane == 0) {
+      tok_kv[t] = p + 1;
+      int page = srow[p / P];
+      slot[t] = page < 0 ? -1 : (int64_t)page * P + (p % P);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Append.  One thread per 16-byte chunk of a (token, kv head) row; K and V in
+// the same thread.  Consecutive threads cover consecutive bytes of a row.
+// ---------------------------------------------------------------------------
+__global__ void k_append(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
+                         const int64_t *__restrict__ slot, int T, uint4 *__restrict__ kp,
+                         uint4 *__restrict__ vp, int num_pages, int Hkv, int P, int chunks_per_row,
+                         int *err) {
+  int64_t total = (int64_t)T * Hkv * chunks_per_row;
+  int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+    int c = (int)(i % chunks_per_row);
+    int64_t th = i / chunks_per_row;
+    int h = (int)(th % Hkv);
+    int t = (int)(th / Hkv);
+    int64_t s = slot[t];
+    if (s < 0) continue;
+    if (s >= (int64_t)num_pages * P) {
+      if (h == 0 && c == 0 && err) atomicOr(err, PA_ERR_SLOT_RANGE);
+      continue;
+    }
+    int64_t page = s / P, off = s % P;
+    int64_t dst = (((page * Hkv) + h) * P + off) * chunks_per_row + c;
+    kp[dst] = k[i];
+    vp[dst] = v[i];
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Validation: every page a token needs must exist; kv_len within the row.
+// ---------------------------------------------------------------------------
+__global__ void k_validate(const int32_t *__restrict__ tpt, int max_pages,
+                           const int32_t *__restrict__ kv, int T, int P, int num_pages, int *err) {
+  int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  int lane = threadIdx.x & 31;
+  int nwarps = (gridDim.x * blockDim.x) >> 5;
+  for (int t = warp; t < T; t += nwarps) {
+    int L = kv[t];
+    if (L < 0 || L > max_pages * P) {
+      if (lane == 0) atomicOr(err, PA_ERR_KV_RANGE);
+      continue;
+    }
+    int np = (L + P - 1) / P;
+    bool bad = false;
+    for (int i = lane; i < np; i += 32) {
+      int pg = tpt[(size_t)t * max_pages + i];
+      bad |= (pg < 0 || pg >= num_pages);
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(err, PA_ERR_PAGE_RANGE);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Planner (one CTA of 1024 threads).
+// ---------------------------------------------------------------------------
+constexpr int kPlanThreads = 1024;
+
+// Exclusive scan across the block; returns the prefix of `v` and writes the
+// block total to *total.  All threads must call it.
+__device__ int block_excl_scan(int v, int *total, int *sh) {
+  int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sh[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    int s = lane < (kPlanThreads / 32) ? sh[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    sh[lane] = s;  // inclusive prefix of warp sums
+  }
+  __syncthreads();
+  int warp_prefix = w > 0 ? sh[w - 1] : 0;
+  *total = sh[kPlanThreads / 32 - 1];
+  __syncthreads();
+  return warp_prefix + x - v;
+}
+
+__global__ void __launch_bounds__(kPlanThreads, 1)
+k_plan(const int32_t *__restrict__ tpt, int max_pages, const int32_t *__restrict__ kv, int T,
+       int P, int Hkv, int min_run, unsigned char *ws, WsLayout lay) {
+  __shared__ int sh[32];
+  WsHeader *hdr = reinterpret_cast<WsHeader *>(ws);
+  int4 *tiles = reinterpret_cast<int4 *>(ws + lay.tiles);
+  int *dec_tok = reinterpret_cast<int *>(ws + lay.dec_tok);
+  int *tok_unit_off = reinterpret_cast<int *>(ws + lay.tok_unit_off);
+  int *flags = reinterpret_cast<int *>(ws + lay.flags);
+  int *runs = reinterpret_cast<int *>(ws + lay.runs);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int cap = max_pages * P;
+
+  if (tid == 0) {
+    hdr->err = 0;
+    hdr->tile_next = 0;
+    hdr->tile_done = 0;
+  }
+  // 1. run starts: token t starts a run unless its row equals row t-1 byte for byte
+  for (int t = warp; t < T; t += kPlanThreads / 32) {
+    bool diff = (t == 0);
+    if (!diff) {
+      const int32_t *a = tpt + (size_t)t * max_pages;
+      const int32_t *b = a - max_pages;
+      bool d = false;
+      for (int i = lane; i < max_pages; i += 32) d |= (a[i] != b[i]);
+      diff = __any_sync(0xffffffffu, d);
+    }
+    if (lane == 0) flags[t] = diff ? 1 : 0;
+  }
+  __syncthreads();
+
+  // 2. run ids by an inclusive scan of the start flags; runs[r] = first token of run r
+  int n_runs = 0;
+  for (int c0 = 0; c0 < T; c0 += kPlanThreads) {
+    int t = c0 + tid;
+    int f = t < T ? flags[t] : 0;
+    int tot;
+    int rid = block_excl_scan(f, &tot, sh) + n_runs;
+    if (f) runs[rid] = t;
+    n_runs += tot;
+  }
+  if (tid == 0) runs[n_runs] = T;
+  __syncthreads();
+
+  // 3. runs of >= min_run tokens become tiles of <= 128 tokens (near-equal
+  //    split); shorter runs become decode tokens.
+  int tile_base = 0, dec_base = 0;
+  for (int c0 = 0; c0 < n_runs; c0 += kPlanThreads) {
+    int r = c0 + tid;
+    int a = 0, len = 0;
+    if (r < n_runs) { a = runs[r]; len = runs[r + 1] - a; }
+    bool prefill_run = r < n_runs && len >= min_run;
+    int n_tiles = prefill_run ? (len + KB - 1) / KB : 0;
+    int n_dec = (r < n_runs && !prefill_run) ? len : 0;
+    int tot_tiles, tot_dec;
+    int tile_off = block_excl_scan(n_tiles, &tot_tiles, sh) + tile_base;
+    int dec_off = block_excl_scan(n_dec, &tot_dec, sh) + dec_base;
+    for (int i = 0; i < n_tiles; ++i) {
+      int b0 = a + (int)((int64_t)len * i / n_tiles);
+      int b1 = a + (int)((int64_t)len * (i + 1) / n_tiles);
+      tiles[tile_off + i] = make_int4(b0, b1 - b0, 0, 0);
+    }
+    for (int i = 0; i < n_dec; ++i) dec_tok[dec_off + i] = a + i;
+    tile_base += tot_tiles;
+    dec_base += tot_dec;
+  }
+  __syncthreads();
+  // 4. key blocks of each tile: ceil(max kv_len over its tokens / 128); one warp per tile
+  for (int i = warp; i < tile_base; i += kPlanThreads / 32) {
+    int4 tl = tiles[i];
+    int mx = 0;
+    bool bad = false;
+    for (int u = tl.x + lane; u < tl.x + tl.y; u += 32) {
+      int L = kv[u];
+      bad |= (L < 0 || L > cap);
+      mx = max(mx, min(max(L, 0), cap));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&hdr->err, PA_ERR_KV_RANGE);
+    if (lane == 0) tiles[i].z = (mx + KB - 1) / KB;
+  }
+  int unit_base = 0;
+  // 3. decode units: 128-key blocks per decode token, prefix-summed
+  for (int c0 = 0; c0 < dec_base; c0 += kPlanThreads) {
+    int i = c0 + tid;
+    int units = 0;
+    if (i < dec_base) {
+      int L = kv[dec_tok[i]];
+      if (L < 0 || L > cap) { atomicOr(&hdr->err, PA_ERR_KV_RANGE); L = L < 0 ? 0 : cap; }
+      units = (L + KB - 1) / KB;
+    }
+    int tot;
+    int off = block_excl_scan(units, &tot, sh) + unit_base;
+    if (i < dec_base) tok_unit_off[i] = off;
+    unit_base += tot;
+    __syncthreads();
+  }
+  if (tid == 0) {
+    tok_unit_off[dec_base] = unit_base;
+    hdr->n_tiles = tile_base;
+    hdr->n_dec = dec_base;
+    hdr->n_units = unit_base * Hkv;
+    hdr->T = T;
+    hdr->Hkv = Hkv;
+    hdr->P = P;
+    hdr->max_pages = max_pages;
+  }
+}
+
+}  // namespace pa

@@ -1,0 +1,39 @@
+// Kernel declarations and launch parameters shared by the translation units.
+#pragma once
+
+#include "common.cuh"
+
+namespace pa {
+
+__global__ void k_expand(const int32_t *seq_pt, int n_seq, int max_pages, const int32_t *tok_seq,
+                         const int32_t *tok_pos, int T, int P, int32_t *tok_pt, int32_t *tok_kv,
+                         int64_t *slot, int *err);
+__global__ void k_append(const uint4 *k, const uint4 *v, const int64_t *slot, int T, uint4 *kp,
+                         uint4 *vp, int num_pages, int Hkv, int P, int chunks_per_row, int *err);
+__global__ void k_validate(const int32_t *tpt, int max_pages, const int32_t *kv, int T, int P,
+                           int num_pages, int *err);
+__global__ void k_plan(const int32_t *tpt, int max_pages, const int32_t *kv, int T, int P, int Hkv,
+                       int min_run, unsigned char *ws, WsLayout lay);
+
+// Arguments of the attention kernels (passed by value).
+struct AttnArgs {
+  const uint16_t *q;
+  const uint16_t *k_pages;
+  const uint16_t *v_pages;
+  const int32_t *tpt;
+  const int32_t *kv;
+  uint16_t *out;
+  unsigned char *ws;
+  WsLayout lay;
+  int max_pages, T, Hq, Hkv, P, D, num_pages;
+  float scale_log2;  // scale * log2(e): softmax evaluated with exp2
+};
+
+// Decode: split-KV over all SMs plus the log-sum-exp reduce.  Returns a
+// cudaError_t from the launches.
+cudaError_t launch_decode(const AttnArgs &a, int num_sms, cudaStream_t s);
+
+// Prefill: tcgen05 tensor-core tiles.
+cudaError_t launch_prefill(const AttnArgs &a, int num_sms, const void *tmaps, cudaStream_t s);
+
+}  // namespace pa
