@@ -1,0 +1,444 @@
+"""Benchmark of the paged-attention hot path on GB300.
+
+One step = one pass of the whole path over one batch of synthetic input:
+  prefill 8x16K (default): the 65 ubatches of 8 x 16384-token prompts, each
+      ubatch = per-token expansion -> reshape-and-cache -> plan -> prefill
+      (tcgen05) + decode (split-KV + reduce) for one Qwen3-8B-shaped layer
+      (32/8 heads, d 128, page 128).  value = causal attention TFLOP/s.
+  decode (reported beside it): 8 sequences, KV length U[1024, 4096], one query
+      token each; expansion + plan once, then 36 layers of append + decode over
+      36 distinct pools (4 GB > L2).  value = algorithmic KV GB/s.
+
+Prints ONE JSON line (rank 0).  --impl reference times the CPU fp64 oracle on
+the same workload (bounded sample per step).  Under torchrun every rank runs its
+own replica (weak scaling; no data-path collective); timings are max-reduced.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode KV GB/s + prefill TFLOP/s, Qwen3-8B-shape paged attn, 8×16K, 1 GB300"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+DECODE_LAYERS = 36
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+        return False
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        mhz = sorted(r[0] for r in rows)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3])
+                          if v.lower() == "active"})
+        return {"sm_mhz": mhz[len(mhz) // 2], "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": max(r[2] for r in rows), "samples": len(rows),
+                "reasons": reasons}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def aggregate(units_per_rank: float, seconds_max: float, world: int) -> float:
+    """Whole-job throughput: units all ranks processed / max-over-ranks time."""
+    return units_per_rank * world / seconds_max
+
+
+# ----------------------------------------------------------------------------- prefill leg
+
+class PrefillBench:
+    def __init__(self, pa, torch, dev, seed=0):
+        import workloads
+        self.pa, self.torch, self.dev = pa, torch, dev
+        self.wl = wl = workloads.Prefill8x16K(seed)
+        t = torch
+        self.spt = t.from_numpy(wl.seq_page_table).to(dev)
+        self.kp = t.full((wl.num_pages, wl.Hkv, wl.P, wl.d), float("nan"), dtype=t.float16,
+                         device=dev)
+        self.vp = t.full_like(self.kp, float("nan"))
+        self.ub = []
+        self.host = []
+        for u in range(len(wl.ubatches)):
+            ts, tp, q, k, v = wl.ubatch(u)
+            h = dict(tok_seq=t.from_numpy(ts).pin_memory(), tok_pos=t.from_numpy(tp).pin_memory(),
+                     q=t.from_numpy(q.view(np.float16)).pin_memory(),
+                     k=t.from_numpy(np.ascontiguousarray(k).view(np.float16)).pin_memory(),
+                     v=t.from_numpy(np.ascontiguousarray(v).view(np.float16)).pin_memory())
+            self.host.append(h)
+            d = {k_: x.to(dev) for k_, x in h.items()}
+            T = ts.shape[0]
+            d["T"] = T
+            d["out"] = t.empty((T, wl.Hq, wl.d), dtype=t.float16, device=dev)
+            d["tpt"] = t.empty((T, wl.max_pages), dtype=t.int32, device=dev)
+            d["kv"] = t.empty(T, dtype=t.int32, device=dev)
+            d["slot"] = t.empty(T, dtype=t.int64, device=dev)
+            d["flops"] = 4.0 * wl.d * wl.Hq * float((tp.astype(np.int64) + 1).sum())
+            self.ub.append(d)
+        self.host_out = [t.empty((d["T"], wl.Hq, wl.d), dtype=t.float16).pin_memory()
+                         for d in self.ub]
+        Tmax = max(d["T"] for d in self.ub)
+        self.ws = pa.new_workspace(Tmax, wl.Hq, wl.Hkv, wl.d, dev)
+        self.flops = sum(d["flops"] for d in self.ub)
+        self.launches_per_step = 6 * len(self.ub)
+
+    def _ubatch(self, d, ev=None):
+        pa, wl = self.pa, self.wl
+        pa.expand_ubatch(self.spt, d["tok_seq"], d["tok_pos"], wl.P, out=(d["tpt"], d["kv"], d["slot"]))
+        pa.kv_append(d["k"], d["v"], d["slot"], self.kp, self.vp)
+        pa.plan(d["tpt"], d["kv"], wl.Hq, wl.Hkv, wl.P, wl.d, self.ws)
+        if ev is not None:
+            ev[0].record()
+        pa.prefill(d["q"], self.kp, self.vp, d["tpt"], d["kv"], wl.scale, d["out"], self.ws)
+        if ev is not None:
+            ev[1].record()
+        pa.decode(d["q"], self.kp, self.vp, d["tpt"], d["kv"], wl.scale, d["out"], self.ws)
+
+    def step(self, events=None):
+        for i, d in enumerate(self.ub):
+            self._ubatch(d, None if events is None else events[i])
+
+    def step_e2e(self):
+        """Same step from pinned host buffers: H2D of each ubatch's inputs, D2H of its output."""
+        t = self.torch
+        h2d = d2h = 0
+        for d, h, ho in zip(self.ub, self.host, self.host_out):
+            for k_ in ("tok_seq", "tok_pos", "q", "k", "v"):
+                d[k_].copy_(h[k_], non_blocking=True)
+                h2d += h[k_].numel() * h[k_].element_size()
+            self._ubatch(d)
+            ho.copy_(d["out"], non_blocking=True)
+            d2h += ho.numel() * ho.element_size()
+        return h2d, d2h
+
+
+# ----------------------------------------------------------------------------- decode leg
+
+class DecodeBench:
+    def __init__(self, pa, torch, dev, seed=0, layers=DECODE_LAYERS):
+        import workloads
+        self.pa, self.torch = pa, torch
+        self.case = c = workloads.decode(seed)
+        t = torch
+        self.spt = t.from_numpy(c.seq_page_table()).to(dev)
+        self.tok_seq = t.from_numpy(c.tok_seq).to(dev)
+        self.tok_pos = t.from_numpy(c.tok_pos).to(dev)
+        kp = t.from_numpy(c.k_pool.view(np.float16)).to(dev)
+        vp = t.from_numpy(c.v_pool.view(np.float16)).to(dev)
+        self.pools = [(kp.clone(), vp.clone()) for _ in range(layers)]
+        self.q = [t.from_numpy(c.q.view(np.float16)).to(dev) for _ in range(layers)]
+        self.kn = t.from_numpy(c.k_new.view(np.float16)).to(dev)
+        self.vn = t.from_numpy(c.v_new.view(np.float16)).to(dev)
+        self.out = [t.empty_like(self.q[0]) for _ in range(layers)]
+        self.ws = pa.new_workspace(c.T, c.Hq, c.Hkv, c.d, dev)
+        self.tpt = t.empty((c.T, c.max_pages), dtype=t.int32, device=dev)
+        self.kv = t.empty(c.T, dtype=t.int32, device=dev)
+        self.slot = t.empty(c.T, dtype=t.int64, device=dev)
+        self.bytes_per_layer = float(c.seq_len.astype(np.int64).sum()) * c.Hkv * c.d * 2 * 2
+        self.layers = layers
+        self.launches_per_step = 2 + 3 * layers
+
+    def step(self, events=None):
+        pa, c = self.pa, self.case
+        pa.expand_ubatch(self.spt, self.tok_seq, self.tok_pos, c.P, out=(self.tpt, self.kv, self.slot))
+        pa.plan(self.tpt, self.kv, c.Hq, c.Hkv, c.P, c.d, self.ws)
+        for l in range(self.layers):
+            kp, vp = self.pools[l]
+            pa.kv_append(self.kn, self.vn, self.slot, kp, vp)
+            if events is not None:
+                events[l][0].record()
+            pa.decode(self.q[l], kp, vp, self.tpt, self.kv, c.scale, self.out[l], self.ws)
+            if events is not None:
+                events[l][1].record()
+
+
+# ----------------------------------------------------------------------------- timing
+
+def time_steps(torch, fn, steps, warmup, world, per_launch=None):
+    """Warm up, then time exactly `steps` calls of fn between barrier+sync pairs.
+    per_launch: number of (start, end) event pairs to record per step (kernel timing)."""
+    for _ in range(warmup):
+        fn(None) if per_launch else fn()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev_pairs = []
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(steps):
+        if per_launch:
+            pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                     for _ in range(per_launch)]
+            ev_pairs.append(pairs)
+            fn(pairs)
+        else:
+            fn()
+    stop.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    total_ms = start.elapsed_time(stop)
+    kern_ms = None
+    if per_launch:
+        kern_ms = sum(a.elapsed_time(b) for pairs in ev_pairs for (a, b) in pairs)
+    return total_ms, kern_ms
+
+
+def cpu_baseline_prefill(wl, budget_s=12.0):
+    """The oracle as it stands on host cores: sampled tokens of the middle
+    ubatches of the 8x16K prefill, growing the sample until ~budget_s of work."""
+    import oracle
+    kp, vp = wl.pool_final()
+    mids = list(range(len(wl.ubatches) // 2, len(wl.ubatches)))
+    flops = 0.0
+    secs = 0.0
+    n_tok = 0
+    stride = 64
+    i = 0
+    while secs < budget_s and i < len(mids):
+        u = mids[i]
+        ts, tp, q, _, _ = wl.ubatch(u)
+        tpt, kv, _ = oracle.expand_ubatch(wl.seq_page_table, ts, tp, wl.P)
+        sel = np.arange(0, ts.shape[0], stride, dtype=np.int32)
+        t0 = time.perf_counter()
+        oracle.paged_attention(q, kp, vp, tpt, kv, wl.scale, tokens=sel)
+        secs += time.perf_counter() - t0
+        flops += 4.0 * wl.d * wl.Hq * float(kv[sel].astype(np.int64).sum())
+        n_tok += len(sel)
+        i += 1
+    return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{n_tok} tokens (every {stride}th) of {i} late ubatches of the 8x16K "
+                      f"prefill, all 32 heads, fp64; {secs:.1f} s of CPU work"}
+
+
+# ----------------------------------------------------------------------------- arms
+
+def run_ours(args):
+    import torch
+    world, rank, local = dist_setup()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", init_method="env://")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import paged_kv_cache_pages_gb300 as pa
+
+    peaks, peak_src = load_peaks()
+    pb = PrefillBench(pa, torch, dev, seed=args.seed)
+    n_ub = len(pb.ub)
+
+    # correctness guard: the run must not report device errors
+    pb.step()
+    torch.cuda.synchronize()
+    if pa.read_error(pb.ws):
+        raise RuntimeError("device error word set during the prefill warm-up")
+
+    with ClockSampler(local) as clk:
+        total_ms, kern_ms = time_steps(torch, pb.step, args.steps, args.warmup, world,
+                                       per_launch=n_ub)
+    clocks = clk.summary()
+    t_step = max_over_ranks(total_ms / 1e3 / args.steps, world)
+    value = aggregate(pb.flops, t_step, world) / 1e12
+    t_kern = kern_ms / 1e3 / (args.steps * n_ub)             # average prefill launch
+    achieved = pb.flops / n_ub / t_kern / 1e12
+    peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+
+    # end to end: pinned host buffers, copies inside the timed region
+    for _ in range(args.warmup):
+        pb.step_e2e()
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    s0 = torch.cuda.Event(enable_timing=True)
+    s1 = torch.cuda.Event(enable_timing=True)
+    s0.record()
+    for _ in range(args.steps):
+        h2d, d2h = pb.step_e2e()
+    s1.record()
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(s0.elapsed_time(s1) / 1e3 / args.steps, world)
+
+    # decode leg
+    db = DecodeBench(pa, torch, dev, seed=args.seed)
+    d_total, d_kern = time_steps(torch, db.step, args.steps, args.warmup, world,
+                                 per_launch=db.layers)
+    d_step = max_over_ranks(d_total / 1e3 / args.steps, world)
+    d_value = aggregate(db.bytes_per_layer * db.layers, d_step, world) / 1e9
+    d_kt = d_kern / 1e3 / (args.steps * db.layers)
+    d_ach = db.bytes_per_layer / d_kt / 1e9
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    if pa.read_error(db.ws) or pa.read_error(pb.ws):
+        raise RuntimeError("device error word set during the timed region")
+
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_step * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic",
+        "config": {"workload": "prefill_8x16k", "n_seq": 8, "prompt_tokens": 16384,
+                   "ubatches": n_ub, "ubatch_tokens_max": 2048, "slots": 4,
+                   "q_heads": 32, "kv_heads": 8, "head_dim": 128, "page_size": 128,
+                   "pool_pages": pb.wl.num_pages, "flops_per_step": pb.flops,
+                   "l2": "inputs larger than L2 (KV pool 655 MB, q 1 GB per step)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "kernel": "k_prefill", "achieved": round(achieved, 2),
+                     "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "peak_source": f"{peak_src} bf16 sustained (f16 dense rate = bf16)",
+                     "traffic": None},
+        "e2e": {"value": round(aggregate(pb.flops, e2e_s, world) / 1e12, 3), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": pb.launches_per_step * args.steps,
+        "clocks": clocks,
+        "decode": {"workload": "decode_8seq", "value": round(d_value, 1), "unit": "GB/s",
+                   "layers": db.layers, "kv_bytes_per_layer": db.bytes_per_layer,
+                   "ms_per_step": round(d_step * 1e3, 3),
+                   "gpu_launches": db.launches_per_step * args.steps,
+                   "roofline": {"bound": "hbm", "kernel": "k_decode + k_reduce",
+                                "achieved": round(d_ach, 1), "peak": hbm, "unit": "GB/s",
+                                "frac": round(d_ach / hbm, 4),
+                                "peak_source": f"{peak_src} hbm copy", "traffic": None}},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_prefill(pb.wl, budget_s=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The CPU fp64 oracle as the reference arm (rank 0 only)."""
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    import workloads
+    wl = workloads.Prefill8x16K(args.seed)
+    for _ in range(args.warmup):
+        cpu_baseline_prefill(wl, budget_s=1.0)
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        vals.append(cpu_baseline_prefill(wl, budget_s=args.cpu_budget / max(args.steps, 1)))
+    wall = time.perf_counter() - t0
+    v = float(np.median([x["value"] for x in vals]))
+    line = {"metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(wall / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": "prefill_8x16k", "n_seq": 8, "prompt_tokens": 16384,
+                       "q_heads": 32, "kv_heads": 8, "head_dim": 128, "page_size": 128,
+                       "parallelism": "host cores"},
+            "cpu_baseline": {"kind": "oracle", "cores": vals[0]["cores"], "value": v,
+                             "unit": "TFLOP/s", "sample": vals[0]["sample"]},
+            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

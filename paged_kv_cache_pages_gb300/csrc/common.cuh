@@ -14,7 +14,7 @@ namespace pa {
 // Workspace layout (device memory owned by the caller).
 //
 //   [0, 256)            WsHeader
-//   tiles               int4 [T]        (tok_start, n_tok, n_kblocks, 0)
+//   tiles               int4 [T]        (tok_start, n_tok, n_kblocks, max kv_len)
 //   dec_tok             int  [T]        decode token indices
 //   tok_unit_off        int  [T + 1]    prefix sums of decode key-blocks per token
 //   flags               int  [T]        plan scratch: run-start flags

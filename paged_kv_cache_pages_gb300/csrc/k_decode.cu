@@ -455,12 +455,18 @@ __global__ void __launch_bounds__(128) k_reduce(AttnArgs a, int C) {
     if (c_first == c_last) continue;  // finished inside one CTA
     for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
       const int h = idx / D, dd = idx - h * D;
+      // only CTAs whose unit range is non-empty wrote a partial (with fewer units
+      // than CTAs, some CTAs in [c_first, c_last] own no unit at all)
+      auto has_units = [&](int cc) {
+        return (int64_t)(cc + 1) * U / C > (int64_t)cc * U / C;
+      };
       float M = -INFINITY;
       for (int cc = c_first; cc <= c_last; ++cc)
-        M = fmaxf(M, partials[((size_t)(ig + cc) * G + h) * (D + 2)]);
+        if (has_units(cc)) M = fmaxf(M, partials[((size_t)(ig + cc) * G + h) * (D + 2)]);
       float o = 0.f, Ls = 0.f;
       if (M != -INFINITY) {
         for (int cc = c_first; cc <= c_last; ++cc) {
+          if (!has_units(cc)) continue;
           const float *pp = partials + ((size_t)(ig + cc) * G + h) * (D + 2);
           float f = exp2_approx(pp[0] - M);
           o += f * pp[2 + dd];

@@ -1,19 +1,488 @@
-// Prefill attention on tcgen05 tensor cores (sm_103a).  Placeholder until the
-// tensor-core kernel lands: flags any planned tile as unsupported.
+// Prefill attention on tcgen05 tensor cores with TMEM accumulators (sm_103a).
+//
+// Work item = (tile of <= 128 consecutive ubatch tokens whose page-table rows
+// are identical, KV head g, pair of query heads of that group).  The two query
+// heads share every K/V tile the CTA loads (GQA grouping), so one 128-key block
+// of K and of V is fetched once for 2 x 128 query rows.
+//
+// Warp roles (384 threads = 3 warpgroups, one CTA per SM, persistent over items):
+//   warps 0-3  softmax of query tile 0 (thread = query row = TMEM lane)
+//   warps 4-7  softmax of query tile 1
+//   warp 8     TMA producer: Q tiles (3-D map over [T][Hq][d]) and, for each
+//              128-key block, the K and V boxes of the tile's pages (2-D map
+//              over the pool rows), 128-byte swizzled, 2-stage ring
+//   warp 9     MMA issuer: S_i = Q_i K^T (SS, f16 -> f32 in TMEM), then
+//              O_i += P_i V with P_i read from TMEM (TS), V MN-major in smem
+//   warps 10-11 idle
+// The softmax warpgroups raise their register budget with setmaxnreg (a
+// 128-column score row lives in registers); the third warpgroup lowers its own.
+// TMEM (512 columns): S0 | S1 | O0 | O1.  P_i (f16) overwrites the first 64
+// columns of S_i.  The issue order PV0(kb), S0(kb+1), PV1(kb), S1(kb+1) lets the
+// softmax of one tile run while the tensor core works on the other.
+//
+// Masking: key j of a block is valid for query row t iff j < tok_kv_len[t]
+// (causal per token).  Scores of invalid keys are replaced by -inf (select, so
+// NaN cells never leak); V rows past the tile's longest kv_len are zeroed in
+// shared memory before the PV product (0 * NaN would poison it).  The softmax
+// is online in base 2 with a lazy rescale: O is rescaled only when a row's max
+// grows by more than 2^8.
+#include "tc.cuh"
 #include "tmap.cuh"
 
 namespace pa {
 
-__global__ void k_prefill_stub(AttnArgs a) {
+constexpr int kPfThreads = 384;
+constexpr int kRegsSoftmax = 192;   // per thread, warpgroups 0 and 1
+constexpr int kRegsOther = 104;     // per thread, warpgroup 2
+// registers the split needs from the launch; checked on the host before launching
+constexpr int kRegsSplitTotal = 2 * 128 * kRegsSoftmax + 128 * kRegsOther;
+constexpr int kPfStages = 2;
+constexpr int kWarpTma = 8;
+constexpr int kWarpMma = 9;
+constexpr int kBoxBytes = 128 * 128;  // 128 rows x 64 halves
+constexpr float kRescaleThreshold = 8.0f;
+
+template <int D>
+struct PfCfg {
+  static constexpr int kHalves = D / 64;
+  static constexpr int kTile = kHalves * kBoxBytes;  // 128 rows x D halves
+  static constexpr int kQ0 = 0;
+  static constexpr int kQ1 = kTile;
+  static constexpr int kK = 2 * kTile;
+  static constexpr int kV = kK + kPfStages * kTile;
+  static constexpr int kBarOff = kV + kPfStages * kTile;
+  static constexpr int kUsed = kBarOff + 256;
+  // at least ~120 KB so that a second CTA never shares the SM (and its TMEM)
+  static constexpr int kSmem = (kUsed < 120 * 1024 ? 120 * 1024 : kUsed) + 1024;
+};
+
+struct PfBars {
+  uint64_t q_full, q_empty;
+  uint64_t k_full[kPfStages], k_empty[kPfStages], v_full[kPfStages], v_empty[kPfStages];
+  uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
+  uint32_t tmem_base;
+  int abort;
+};
+
+// Bounded wait that also gives up as soon as another role of the CTA gave up.
+__device__ __forceinline__ bool pf_wait(uint64_t *bar, uint32_t parity, int *err,
+                                        volatile int *abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if ((it & 127u) == 127u && globaltimer_ns() - t0 > kWaitLimitNs) {
+      atomicOr(err, PA_ERR_TIMEOUT);
+      *abort = 1;
+      return false;
+    }
+  }
+}
+
+struct Item {
+  int tile_start, n_tok, nkb, max_kv, g, h0, h1;
+};
+
+__device__ __forceinline__ Item decode_item(int item, const int4 *tiles, int Hkv, int G) {
+  const int NP = G >= 2 ? G / 2 : 1;
+  Item it;
+  int tile = item / (Hkv * NP);
+  int rem = item - tile * Hkv * NP;
+  it.g = rem / NP;
+  int pair = rem - it.g * NP;
+  int4 tl = tiles[tile];
+  it.tile_start = tl.x;
+  it.n_tok = tl.y;
+  it.nkb = tl.z;
+  it.max_kv = tl.w;
+  it.h0 = G >= 2 ? it.g * G + 2 * pair : it.g;
+  it.h1 = it.h0 + 1;
+  return it;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kPfThreads, 1)
+k_prefill(AttnArgs a, const __grid_constant__ PrefillMaps maps) {
+  using Cfg = PfCfg<D>;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const uint32_t raw_s = smem_u32(smem_raw);
+  unsigned char *smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
+  PfBars *bars = reinterpret_cast<PfBars *>(smem + Cfg::kBarOff);
+
   WsHeader *hdr = reinterpret_cast<WsHeader *>(a.ws);
-  if (hdr->n_tiles > 0 && threadIdx.x == 0) atomicOr(&hdr->err, PA_ERR_TIMEOUT);
+  int *err = &hdr->err;
+  const int4 *tiles = reinterpret_cast<const int4 *>(a.ws + a.lay.tiles);
+  const int G = a.Hq / a.Hkv;
+  const int NQ = G >= 2 ? 2 : 1;
+  const int NP = G >= 2 ? G / 2 : 1;
+  const int n_items = hdr->n_tiles * a.Hkv * NP;
+  if ((int)blockIdx.x >= n_items) return;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 1);
+    for (int s = 0; s < kPfStages; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->s_full[i], 1);
+      mbar_init(&bars->p_full[i], 128);
+      mbar_init(&bars->o_full[i], 1);
+      mbar_init(&bars->o_empty[i], 128);
+    }
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(&bars->tmem_base, 512);
+    tc::tmem_relinquish();
+  }
+  if (warp == kWarpTma && lane == 0) {
+    tc::prefetch_tmap(&maps.q);
+    tc::prefetch_tmap(&maps.k);
+    tc::prefetch_tmap(&maps.v);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = bars->tmem_base;
+  volatile int *abort = &bars->abort;
+  const int cap = a.max_pages * a.P;
+
+  if (warp >= 8) {
+   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
+   if (warp == kWarpTma && lane == 0) {
+    // ------------------------------------------------------------ TMA producer
+    {
+      uint32_t it = 0;
+      int nitem = 0;
+      const int pages_per_block = KB / a.P;
+      const int oob_row = a.num_pages * a.Hkv * a.P;  // first row past the pool: zero fill
+      for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+        Item w = decode_item(item, tiles, a.Hkv, G);
+        if (w.nkb == 0) continue;
+        if (nitem > 0 && !pf_wait(&bars->q_empty, (nitem - 1) & 1, err, abort)) break;
+        mbar_arrive_expect_tx(&bars->q_full, NQ * Cfg::kTile);
+        for (int hf = 0; hf < Cfg::kHalves; ++hf) {
+          tc::tma_load_3d(smem + Cfg::kQ0 + hf * kBoxBytes, &maps.q, hf * 64, w.h0, w.tile_start,
+                          &bars->q_full);
+          if (NQ == 2)
+            tc::tma_load_3d(smem + Cfg::kQ1 + hf * kBoxBytes, &maps.q, hf * 64, w.h1,
+                            w.tile_start, &bars->q_full);
+        }
+        const int32_t *row = a.tpt + (size_t)w.tile_start * a.max_pages;
+        bool ok = true;
+        for (int kb = 0; kb < w.nkb && ok; ++kb, ++it) {
+          const int st = it % kPfStages;
+          const uint32_t ph = (it / kPfStages) & 1u;
+          const int keys = min(KB, w.max_kv - kb * KB);
+          const int npg = (keys + a.P - 1) / a.P;
+          const uint32_t bytes = (uint32_t)npg * a.P * 128u * Cfg::kHalves;
+          // row coordinate of page j of this block in the pool map (past the end when invalid:
+          // the box is zero-filled and nothing outside the pool is touched)
+          auto ycoord = [&](int j) {
+            int page = row[kb * pages_per_block + j];
+            if (page < 0 || page >= a.num_pages) {
+              atomicOr(err, PA_ERR_PAGE_RANGE);
+              return oob_row;
+            }
+            return (page * a.Hkv + w.g) * a.P;
+          };
+          if (!pf_wait(&bars->k_empty[st], ph ^ 1u, err, abort)) { ok = false; break; }
+          mbar_arrive_expect_tx(&bars->k_full[st], bytes);
+          for (int j = 0; j < npg; ++j)
+            for (int hf = 0; hf < Cfg::kHalves; ++hf)
+              tc::tma_load_2d(smem + Cfg::kK + st * Cfg::kTile + hf * kBoxBytes + j * a.P * 128,
+                              &maps.k, hf * 64, ycoord(j), &bars->k_full[st]);
+          if (!pf_wait(&bars->v_empty[st], ph ^ 1u, err, abort)) { ok = false; break; }
+          mbar_arrive_expect_tx(&bars->v_full[st], bytes);
+          for (int j = 0; j < npg; ++j)
+            for (int hf = 0; hf < Cfg::kHalves; ++hf)
+              tc::tma_load_2d(smem + Cfg::kV + st * Cfg::kTile + hf * kBoxBytes + j * a.P * 128,
+                              &maps.v, hf * 64, ycoord(j), &bars->v_full[st]);
+        }
+        if (!ok) break;
+        ++nitem;
+      }
+    }
+   } else if (warp == kWarpMma) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idS = tc::idesc_f16(128, 128, false);
+    constexpr uint32_t idPV = tc::idesc_f16(128, D, true);
+    const uint32_t sQ0 = smem_u32(smem + Cfg::kQ0), sQ1 = smem_u32(smem + Cfg::kQ1);
+    const uint32_t sK = smem_u32(smem + Cfg::kK), sV = smem_u32(smem + Cfg::kV);
+    auto issue_S = [&](int i, int st) {
+      const uint32_t d = tmem + i * 128;
+      const uint32_t kb = sK + st * Cfg::kTile;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk / 4) * kBoxBytes + (kk % 4) * 32;
+        tc::mma_ss(d, tc::sdesc_sw128((i ? sQ1 : sQ0) + off, 16, 1024),
+                   tc::sdesc_sw128(kb + off, 16, 1024),
+                   idS, kk > 0 ? 1u : 0u);
+      }
+    };
+    auto issue_PV = [&](int i, int st, bool acc) {
+      const uint32_t d = tmem + 256 + i * D;
+      const uint32_t p = tmem + i * 128;
+      const uint32_t vb = sV + st * Cfg::kTile;
+#pragma unroll
+      for (int kk = 0; kk < KB / 16; ++kk)
+        tc::mma_ts(d, p + kk * 8, tc::sdesc_sw128(vb + kk * 2048, kBoxBytes, 1024), idPV,
+                   (acc || kk > 0) ? 1u : 0u);
+    };
+    const bool leader = lane == 0;
+    uint32_t it = 0, sc = 0;
+    int nitem = 0;
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+      Item w = decode_item(item, tiles, a.Hkv, G);
+      if (w.nkb == 0) continue;
+      bool ok = pf_wait(&bars->q_full, nitem & 1, err, abort);
+      const int st0 = it % kPfStages;
+      ok = ok && pf_wait(&bars->k_full[st0], (it / kPfStages) & 1u, err, abort);
+      if (!ok) break;
+      tc::fence_after_sync();
+      if (leader) {
+        issue_S(0, st0);
+        tc::commit(&bars->s_full[0]);
+        if (NQ == 2) {
+          issue_S(1, st0);
+          tc::commit(&bars->s_full[1]);
+        }
+        tc::commit(&bars->k_empty[st0]);
+      }
+      __syncwarp();
+      for (int kb = 0; kb < w.nkb; ++kb) {
+        const uint32_t cur = it + kb;
+        const int st = cur % kPfStages;
+        const bool last = kb + 1 == w.nkb;
+        if (!pf_wait(&bars->v_full[st], (cur / kPfStages) & 1u, err, abort)) { ok = false; break; }
+        const int nvalid = w.max_kv - kb * KB;
+        if (last && nvalid < KB) {
+          // zero V rows nvalid..127 in each 64-column box (rows are 128 B, whole rows
+          // are zeroed so the swizzle inside a row does not matter)
+          for (int hf = 0; hf < Cfg::kHalves; ++hf) {
+            uint4 *base = reinterpret_cast<uint4 *>(smem + Cfg::kV + st * Cfg::kTile +
+                                                    hf * kBoxBytes + nvalid * 128);
+            const int n16 = (KB - nvalid) * 8;
+            for (int x = lane; x < n16; x += 32) base[x] = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async();
+        }
+        __syncwarp();
+        if (!pf_wait(&bars->p_full[0], (sc + kb) & 1u, err, abort)) { ok = false; break; }
+        if (kb == 0 && nitem > 0 && !pf_wait(&bars->o_empty[0], (nitem - 1) & 1, err, abort)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        if (leader) {
+          issue_PV(0, st, kb > 0);
+          if (last) tc::commit(&bars->o_full[0]);
+        }
+        __syncwarp();
+        int st2 = 0;
+        if (!last) {
+          const uint32_t nxt = cur + 1;
+          st2 = nxt % kPfStages;
+          if (!pf_wait(&bars->k_full[st2], (nxt / kPfStages) & 1u, err, abort)) { ok = false; break; }
+          tc::fence_after_sync();
+          if (leader) {
+            issue_S(0, st2);
+            tc::commit(&bars->s_full[0]);
+          }
+          __syncwarp();
+        }
+        if (NQ == 2) {
+          if (!pf_wait(&bars->p_full[1], (sc + kb) & 1u, err, abort)) { ok = false; break; }
+          if (kb == 0 && nitem > 0 && !pf_wait(&bars->o_empty[1], (nitem - 1) & 1, err, abort)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          if (leader) {
+            issue_PV(1, st, kb > 0);
+            if (last) tc::commit(&bars->o_full[1]);
+          }
+        }
+        if (leader) {
+          tc::commit(&bars->v_empty[st]);
+          if (!last) {
+            if (NQ == 2) {
+              issue_S(1, st2);
+              tc::commit(&bars->s_full[1]);
+            }
+            tc::commit(&bars->k_empty[st2]);
+          }
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (leader) tc::commit(&bars->q_empty);
+      __syncwarp();
+      it += w.nkb;
+      sc += w.nkb;
+      ++nitem;
+    }
+   }
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+    const int wg = warp >> 2;
+    const int wl = warp & 3;
+    const int row = wl * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(wl * 32) << 16;
+    const uint32_t tS = tmem + wg * 128 + lane_off;
+    const uint32_t tO = tmem + 256 + wg * D + lane_off;
+    if (wg < NQ) {
+      uint32_t sc = 0;
+      int nitem = 0;
+      for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+        Item w = decode_item(item, tiles, a.Hkv, G);
+        const int h = wg ? w.h1 : w.h0;
+        const int tok = w.tile_start + row;
+        const bool valid = row < w.n_tok;
+        const int L = valid ? min(max(a.kv[tok], 0), cap) : 0;
+        uint4 *orow = reinterpret_cast<uint4 *>(a.out + ((size_t)tok * a.Hq + h) * D);
+        if (w.nkb == 0) {
+          if (valid)
+            for (int x = 0; x < D / 8; ++x) orow[x] = make_uint4(0, 0, 0, 0);
+          continue;
+        }
+        float m_run = -INFINITY, l_run = 0.f;
+        bool ok = true;
+        for (int kb = 0; kb < w.nkb; ++kb) {
+          if (!pf_wait(&bars->s_full[wg], (sc + kb) & 1u, err, abort)) { ok = false; break; }
+          tc::fence_after_sync();
+          uint32_t s[4][32];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tc::ld32(tS + c * 32, s[c]);
+          tc::wait_ld();
+          const int nv = min(max(L - kb * KB, 0), KB);
+          float mx = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float x = (c * 32 + j < nv) ? __uint_as_float(s[c][j]) * a.scale_log2
+                                                 : -INFINITY;
+              s[c][j] = __float_as_uint(x);
+              mx = fmaxf(mx, x);
+            }
+          const float m_new = fmaxf(m_run, mx);
+          const bool need = m_new > m_run + kRescaleThreshold;
+          float alpha = 1.f;
+          if (need) {
+            alpha = exp2_approx(m_run - m_new);
+            m_run = m_new;
+          }
+          float rs = 0.f;
+          uint32_t pk[2][32];
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              const float x0 = __uint_as_float(s[c][j]), x1 = __uint_as_float(s[c][j + 1]);
+              const float p0 = x0 == -INFINITY ? 0.f : exp2_approx(x0 - m_run);
+              const float p1 = x1 == -INFINITY ? 0.f : exp2_approx(x1 - m_run);
+              rs += p0 + p1;
+              __half2 hp = __floats2half2_rn(p0, p1);
+              pk[c >> 1][(c & 1) * 16 + (j >> 1)] = *reinterpret_cast<uint32_t *>(&hp);
+            }
+          l_run = l_run * alpha + rs;
+          tc::st32(tS, pk[0]);
+          tc::st32(tS + 32, pk[1]);
+          if (kb > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t o[32];
+              tc::ld32(tO + c * 32, o);
+              tc::wait_ld();
+#pragma unroll
+              for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+              tc::st32(tO + c * 32, o);
+            }
+          }
+          tc::wait_st();
+          tc::fence_before_sync();
+          mbar_arrive(&bars->p_full[wg]);
+        }
+        if (!ok) break;
+        if (!pf_wait(&bars->o_full[wg], nitem & 1, err, abort)) break;
+        tc::fence_after_sync();
+        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tc::ld32(tO + c * 32, o);
+          tc::wait_ld();
+          if (valid) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint32_t hw[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                __half2 hv = __floats2half2_rn(__uint_as_float(o[q * 8 + 2 * e]) * inv,
+                                               __uint_as_float(o[q * 8 + 2 * e + 1]) * inv);
+                hw[e] = *reinterpret_cast<uint32_t *>(&hv);
+              }
+              orow[c * 4 + q] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            }
+          }
+        }
+        tc::fence_before_sync();
+        mbar_arrive(&bars->o_empty[wg]);
+        sc += w.nkb;
+        ++nitem;
+      }
+    }
+  }
+
+  __syncthreads();
+  if (*abort && warp == kWarpMma && lane == 0) {
+    // a role gave up: let the tensor pipe drain (bounded) before TMEM is freed
+    tc::commit(&bars->q_empty);
+    uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 1000000ull) {
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+static cudaError_t launch_prefill_t(const AttnArgs &a, int num_sms, const PrefillMaps *maps,
+                                    cudaStream_t s) {
+  using Cfg = PfCfg<D>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    // setmaxnreg.inc can only draw on registers the block was launched with: refuse to
+    // launch (rather than wait forever) if the compiled allocation does not cover the split
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, k_prefill<D>);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs * kPfThreads < kRegsSplitTotal) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(k_prefill<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  k_prefill<D><<<num_sms, kPfThreads, Cfg::kSmem, s>>>(a, *maps);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_prefill(const AttnArgs &a, int num_sms, const void *tmaps, cudaStream_t s) {
-  (void)num_sms;
-  (void)tmaps;
-  k_prefill_stub<<<1, 32, 0, s>>>(a);
-  return cudaGetLastError();
+  const PrefillMaps *maps = static_cast<const PrefillMaps *>(tmaps);
+  if (a.D == 128) return launch_prefill_t<128>(a, num_sms, maps, s);
+  if (a.D == 64) return launch_prefill_t<64>(a, num_sms, maps, s);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace pa

@@ -207,7 +207,10 @@ k_plan(const int32_t *__restrict__ tpt, int max_pages, const int32_t *__restrict
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&hdr->err, PA_ERR_KV_RANGE);
-    if (lane == 0) tiles[i].z = (mx + KB - 1) / KB;
+    if (lane == 0) {
+      tiles[i].z = (mx + KB - 1) / KB;
+      tiles[i].w = mx;
+    }
   }
   int unit_base = 0;
   // 3. decode units: 128-key blocks per decode token, prefix-summed

@@ -1,0 +1,101 @@
+"""Small, self-contained cases for kernel profiling (ncu) and quick timing.
+
+  python -m paged_kv_cache_pages_gb300.profile_case prefill [--ubatch U] [--reps R]
+      one ubatch of the 8 x 16K prefill (default: a late one, long contexts):
+      expand -> append -> plan -> prefill -> decode, R times.  Device memory:
+      the 655 MB KV pool (larger than L2) plus one ubatch.
+  python -m paged_kv_cache_pages_gb300.profile_case decode [--reps R]
+      the 8-sequence decode layer: expand -> plan -> append -> decode.
+
+Prints the average time of the attention call (CUDA events) and exits 0.
+"""
+import argparse
+import os
+import sys
+
+import numpy as np
+import torch
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+
+import paged_kv_cache_pages_gb300 as pa  # noqa: E402
+import workloads  # noqa: E402
+
+
+def _time(fn, reps):
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    fn()
+    torch.cuda.synchronize()
+    s.record()
+    for _ in range(reps):
+        fn()
+    e.record()
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / reps
+
+
+def prefill(ubatch: int, reps: int):
+    wl = workloads.Prefill8x16K(0)
+    kp_h, vp_h = wl.pool_final()
+    dev = "cuda"
+    kp = torch.from_numpy(kp_h.view(np.float16)).to(dev)
+    vp = torch.from_numpy(vp_h.view(np.float16)).to(dev)
+    ts, tp, q, k, v = wl.ubatch(ubatch)
+    spt = torch.from_numpy(wl.seq_page_table).to(dev)
+    ts_d, tp_d = torch.from_numpy(ts).to(dev), torch.from_numpy(tp).to(dev)
+    q_d = torch.from_numpy(q.view(np.float16)).to(dev)
+    k_d = torch.from_numpy(np.ascontiguousarray(k).view(np.float16)).to(dev)
+    v_d = torch.from_numpy(np.ascontiguousarray(v).view(np.float16)).to(dev)
+    out = torch.empty_like(q_d)
+    ws = pa.new_workspace(ts.shape[0], wl.Hq, wl.Hkv, wl.d, dev)
+    tpt, kv, slot = pa.expand_ubatch(spt, ts_d, tp_d, wl.P)
+    pa.kv_append(k_d, v_d, slot, kp, vp)
+    pa.plan(tpt, kv, wl.Hq, wl.Hkv, wl.P, wl.d, ws)
+
+    def fn():
+        pa.prefill(q_d, kp, vp, tpt, kv, wl.scale, out, ws)
+        pa.decode(q_d, kp, vp, tpt, kv, wl.scale, out, ws)
+
+    ms = _time(fn, reps)
+    if pa.read_error(ws):
+        raise SystemExit("device error word set")
+    flops = 4.0 * wl.d * wl.Hq * float((tp.astype(np.int64) + 1).sum())
+    print(f"prefill ubatch {ubatch}: T={ts.shape[0]} {ms * 1e3:.1f} us/call "
+          f"{flops / ms / 1e9:.1f} TFLOP/s (prefill+decode calls)")
+
+
+def decode(reps: int):
+    c = workloads.decode(0)
+    dev = "cuda"
+    spt = torch.from_numpy(c.seq_page_table()).to(dev)
+    kp = torch.from_numpy(c.k_pool.view(np.float16)).to(dev)
+    vp = torch.from_numpy(c.v_pool.view(np.float16)).to(dev)
+    q = torch.from_numpy(c.q.view(np.float16)).to(dev)
+    tpt, kv, slot = pa.expand_ubatch(spt, torch.from_numpy(c.tok_seq).to(dev),
+                                     torch.from_numpy(c.tok_pos).to(dev), c.P)
+    pa.kv_append(torch.from_numpy(c.k_new.view(np.float16)).to(dev),
+                 torch.from_numpy(c.v_new.view(np.float16)).to(dev), slot, kp, vp)
+    ws = pa.new_workspace(c.T, c.Hq, c.Hkv, c.d, dev)
+    out = torch.empty_like(q)
+    pa.plan(tpt, kv, c.Hq, c.Hkv, c.P, c.d, ws)
+    ms = _time(lambda: pa.decode(q, kp, vp, tpt, kv, c.scale, out, ws), reps)
+    if pa.read_error(ws):
+        raise SystemExit("device error word set")
+    nbytes = float(c.seq_len.astype(np.int64).sum()) * c.Hkv * c.d * 4
+    print(f"decode: {ms * 1e3:.1f} us/call {nbytes / ms / 1e6:.1f} GB/s (L2-warm, one pool)")
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("case", choices=["prefill", "decode"])
+    ap.add_argument("--ubatch", type=int, default=48)
+    ap.add_argument("--reps", type=int, default=3)
+    a = ap.parse_args()
+    if a.case == "prefill":
+        prefill(a.ubatch, a.reps)
+    else:
+        decode(a.reps)
+
+
+if __name__ == "__main__":
+    main()
