@@ -169,6 +169,29 @@ int paged_attn_forward(const uint16_t *q, const uint16_t *k_pages, const uint16_
                        uint16_t *out, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * paged_attn_forward without a caller-provided workspace, for callers that
+ * cannot allocate device memory (a host framework that owns all device memory,
+ * a fixed up-front memory budget, a latency-critical path where an allocation
+ * could synchronise the device).  The pages have no counterpart of this call;
+ * it exists only for such callers.
+ *
+ * Same arguments and result as paged_attn_forward, minus workspace.  The
+ * scratch is one fixed 16 MiB array in device memory inside this library,
+ * held by every GPU that loads the library until the process exits; the call
+ * allocates nothing.  A ubatch whose paged_attn_workspace_size(T, Hq, Hkv, d)
+ * exceeds 16 MiB is rejected with PA_EWORKSPACE (about 980 tokens at 32/8
+ * heads, d 128).  The first call on each device looks up the array's device
+ * address; make that first call before any stream capture.  Every call shares
+ * the array and it keeps the last call's contents (each call clears what it
+ * needs); calls that overlap on the GPU race and must be serialised.  The
+ * device error word of these calls is not exposed.
+ */
+int paged_attn_forward_noalloc(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
+                               const int32_t *tok_page_table, int max_pages,
+                               const int32_t *tok_kv_len, int T, int Hq, int Hkv, int P, int d,
+                               int num_pages, float scale, uint16_t *out, void *stream);
+
+/*
  * Check the tables without trapping: every page id a token needs
  * (row[0 .. ceil(kv_len/P)-1]) must lie in [0, num_pages) and 0 <= kv_len <=
  * max_pages * P.  OR-s PA_ERR_PAGE_RANGE / PA_ERR_KV_RANGE into *err (device).
