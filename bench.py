@@ -162,7 +162,7 @@ class PrefillBench:
         Tmax = max(d["T"] for d in self.ub)
         self.ws = pa.new_workspace(Tmax, wl.Hq, wl.Hkv, wl.d, dev)
         self.flops = sum(d["flops"] for d in self.ub)
-        self.launches_per_step = 6 * len(self.ub)
+        self.launches_per_step = 7 * len(self.ub)   # expand, append, plan x2, prefill, decode, reduce
 
     def _ubatch(self, d, ev=None):
         pa, wl = self.pa, self.wl
@@ -218,7 +218,7 @@ class DecodeBench:
         self.slot = t.empty(c.T, dtype=t.int64, device=dev)
         self.bytes_per_layer = float(c.seq_len.astype(np.int64).sum()) * c.Hkv * c.d * 2 * 2
         self.layers = layers
-        self.launches_per_step = 2 + 3 * layers
+        self.launches_per_step = 3 + 3 * layers   # expand, plan x2; per layer append, decode, reduce
 
     def step(self, events=None):
         pa, c = self.pa, self.case
@@ -265,6 +265,22 @@ def time_steps(torch, fn, steps, warmup, world, per_launch=None):
     if per_launch:
         kern_ms = sum(a.elapsed_time(b) for pairs in ev_pairs for (a, b) in pairs)
     return total_ms, kern_ms
+
+
+def capture_step(torch, fn):
+    """One step captured as a CUDA graph (the same launches, replayed without
+    host launch overhead)."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fn()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
 
 
 def cpu_baseline_prefill(wl, budget_s=12.0):
@@ -318,9 +334,10 @@ def run_ours(args):
     if pa.read_error(pb.ws):
         raise RuntimeError("device error word set during the prefill warm-up")
 
+    graph = capture_step(torch, pb.step)
     with ClockSampler(local) as clk:
-        total_ms, kern_ms = time_steps(torch, pb.step, args.steps, args.warmup, world,
-                                       per_launch=n_ub)
+        total_ms, _ = time_steps(torch, graph.replay, args.steps, args.warmup, world)
+        _, kern_ms = time_steps(torch, pb.step, args.steps, args.warmup, world, per_launch=n_ub)
     clocks = clk.summary()
     t_step = max_over_ranks(total_ms / 1e3 / args.steps, world)
     value = aggregate(pb.flops, t_step, world) / 1e12
@@ -345,8 +362,9 @@ def run_ours(args):
 
     # decode leg
     db = DecodeBench(pa, torch, dev, seed=args.seed)
-    d_total, d_kern = time_steps(torch, db.step, args.steps, args.warmup, world,
-                                 per_launch=db.layers)
+    d_graph = capture_step(torch, db.step)
+    d_total, _ = time_steps(torch, d_graph.replay, args.steps, args.warmup, world)
+    _, d_kern = time_steps(torch, db.step, args.steps, args.warmup, world, per_launch=db.layers)
     d_step = max_over_ranks(d_total / 1e3 / args.steps, world)
     d_value = aggregate(db.bytes_per_layer * db.layers, d_step, world) / 1e9
     d_kt = d_kern / 1e3 / (args.steps * db.layers)
@@ -373,6 +391,8 @@ def run_ours(args):
         "e2e": {"value": round(aggregate(pb.flops, e2e_s, world) / 1e12, 3), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": pb.launches_per_step * args.steps,
+        "timing": "value: CUDA-graph replay of whole steps; roofline: per-launch CUDA events "
+                  "in a non-graph pass of the same steps",
         "clocks": clocks,
         "decode": {"workload": "decode_8seq", "value": round(d_value, 1), "unit": "GB/s",
                    "layers": db.layers, "kv_bytes_per_layer": db.bytes_per_layer,

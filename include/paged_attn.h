@@ -176,11 +176,11 @@ int paged_attn_forward(const uint16_t *q, const uint16_t *k_pages, const uint16_
  * it exists only for such callers.
  *
  * Same arguments and result as paged_attn_forward, minus workspace.  The
- * scratch is one fixed 16 MiB array in device memory inside this library,
+ * scratch is one fixed 64 MiB array in device memory inside this library,
  * held by every GPU that loads the library until the process exits; the call
  * allocates nothing.  A ubatch whose paged_attn_workspace_size(T, Hq, Hkv, d)
- * exceeds 16 MiB is rejected with PA_EWORKSPACE (about 980 tokens at 32/8
- * heads, d 128).  The first call on each device looks up the array's device
+ * exceeds 64 MiB is rejected with PA_EWORKSPACE (about 4000 tokens at 32/8
+ * heads, d 128, on 152 SMs).  The first call on each device looks up the array's device
  * address; make that first call before any stream capture.  Every call shares
  * the array and it keeps the last call's contents (each call clears what it
  * needs); calls that overlap on the GPU race and must be serialised.  The

@@ -161,11 +161,19 @@ int paged_attn_plan(const int32_t *tok_page_table, int max_pages, const int32_t 
                       P, d, 1, nullptr, workspace, workspace_bytes, false);
   if (st != PA_OK) return st;
   if (T == 0) return PA_OK;
-  WsLayout lay = ws_layout(T, Hq, Hkv, d, sm_count());
+  const int C = sm_count();
+  WsLayout lay = ws_layout(T, Hq, Hkv, d, C);
+  const int G = Hq / Hkv;
+  const int NP = G >= 2 ? G / 2 : 1;
   int min_run = g_min_run.load();
-  k_plan<<<1, 1024, 0, static_cast<cudaStream_t>(stream)>>>(
-      tok_page_table, max_pages, tok_kv_len, T, P, Hkv, min_run,
-      static_cast<unsigned char *>(workspace), lay);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned char *ws = static_cast<unsigned char *>(workspace);
+  int blocks = (T + 7) / 8;
+  if (blocks > 65535) blocks = 65535;
+  k_plan_mark<<<blocks, 256, 0, s>>>(tok_page_table, max_pages, T, ws, lay);
+  if (cudaGetLastError() != cudaSuccess) return PA_ELAUNCH;
+  k_plan<<<1, 1024, 0, s>>>(tok_page_table, max_pages, tok_kv_len, T, P, Hkv, NP, min_run, C, ws,
+                            lay);
   return launch_status(cudaGetLastError());
 }
 

@@ -13,21 +13,30 @@ namespace pa {
 // ----------------------------------------------------------------------------
 // Workspace layout (device memory owned by the caller).
 //
-//   [0, 256)            WsHeader
-//   tiles               int4 [T]        (tok_start, n_tok, n_kblocks, max kv_len)
-//   dec_tok             int  [T]        decode token indices
-//   tok_unit_off        int  [T + 1]    prefix sums of decode key-blocks per token
-//   flags               int  [T]        plan scratch: run-start flags
-//   runs                int  [T + 1]    plan scratch: first token of each run
-//   partials            float[(T*Hkv + C)][G][D + 2]   split-KV partial results
+//   [0, 256)       WsHeader
+//   tiles          int4 [T]      (tok_start, n_tok, n_kblocks, max kv_len)
+//   dec_tok        int  [T]      decode token indices
+//   tok_unit_off   int  [T + 1]  prefix sums of decode key blocks per token
+//   flags          int  [T]      plan scratch: run-start flags
+//   runs           int  [T + 1]  plan scratch: first token of each run
+//   tile_off       int  [T + 1]  prefix sums of prefill work (key blocks x items) per tile
+//   dec_start      int4 [C]      first decode unit of each CTA: (i, g, kb, -)
+//   pf_start       int4 [C]      first prefill unit of each CTA: (tile, item in tile, kb, -)
+//   pf_cnt         int  [T * Hkv * NP * 2 * 4]  arrival counters of split prefill items,
+//                                  one per (item, softmax warpgroup, warp)
+//   partials       union of
+//                    decode split partials  float [(T*Hkv + C)][G][D + 2]
+//                    prefill split parts    float [2C][2][128][D + 4]  (16-byte rows)
+// The decode and prefill kernels of one ubatch run one after the other on a
+// stream, so their partials share one region.
 // ----------------------------------------------------------------------------
 struct WsHeader {
-  int err;           // PA_ERR_* bits
-  int n_tiles;       // prefill tiles
-  int n_dec;         // decode tokens
-  int n_units;       // decode work units (token, kv head, 128-key block)
-  int tile_next;     // dynamic prefill scheduler: next work item
-  int tile_done;     // CTAs finished (last one resets tile_next)
+  int err;        // PA_ERR_* bits
+  int n_tiles;    // prefill tiles
+  int n_dec;      // decode tokens
+  int n_units;    // decode work units (token, kv head, 128-key block)
+  int pf_work;    // prefill work units (item, 128-key block)
+  int C;          // CTAs the plan was cut for (= SM count)
   int T, Hq, Hkv, D, P, max_pages;
   int pad[52];
 };
@@ -36,7 +45,9 @@ static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 constexpr int KB = 128;  // keys per block (decode unit and prefill key tile)
 
 struct WsLayout {
-  size_t tiles, dec_tok, tok_unit_off, flags, runs, partials, total;
+  size_t tiles, dec_tok, tok_unit_off, flags, runs, tile_off, dec_start, pf_start, pf_cnt;
+  size_t partials, total;
+  int n_cnt;  // entries of pf_cnt
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -45,16 +56,32 @@ __host__ __device__ inline WsLayout ws_layout(int T, int Hq, int Hkv, int D, int
   WsLayout l;
   size_t o = sizeof(WsHeader);
   size_t Tm = T > 0 ? (size_t)T : 1;
+  size_t G = (size_t)(Hq / Hkv);
+  size_t NP = G >= 2 ? G / 2 : 1;
   l.tiles = o;        o = align_up(o + Tm * 16, 256);
   l.dec_tok = o;      o = align_up(o + Tm * 4, 256);
   l.tok_unit_off = o; o = align_up(o + (Tm + 1) * 4, 256);
   l.flags = o;        o = align_up(o + Tm * 4, 256);
   l.runs = o;         o = align_up(o + (Tm + 1) * 4, 256);
+  l.tile_off = o;     o = align_up(o + (Tm + 1) * 4, 256);
+  l.dec_start = o;    o = align_up(o + (size_t)C * 16, 256);
+  l.pf_start = o;     o = align_up(o + (size_t)C * 16, 256);
+  l.n_cnt = (int)(Tm * Hkv * NP * 8);
+  l.pf_cnt = o;       o = align_up(o + (size_t)l.n_cnt * 4, 256);
   l.partials = o;
-  size_t G = (size_t)(Hq / Hkv);
-  o = align_up(o + (Tm * Hkv + (size_t)C) * G * (D + 2) * 4, 256);
+  size_t dec_part = (Tm * Hkv + (size_t)C) * G * (D + 2) * 4;
+  size_t pf_part = (size_t)2 * C * 2 * 128 * (D + 4) * 4;
+  o = align_up(o + (dec_part > pf_part ? dec_part : pf_part), 256);
   l.total = o;
   return l;
+}
+
+// The CTA (of C, each owning [floor(cW/C), floor((c+1)W/C))) that owns unit u.
+__host__ __device__ inline int cta_of_unit(long long u, long long W, int C) {
+  return (int)(((u + 1) * C + W - 1) / W) - 1;
+}
+__host__ __device__ inline bool cta_has_units(int c, long long W, int C) {
+  return (long long)(c + 1) * W / C > (long long)c * W / C;
 }
 
 // ----------------------------------------------------------------------------
@@ -137,14 +164,34 @@ __device__ __forceinline__ float exp2_approx(float x) {
   return y;
 }
 
-// Two fp32 FMAs in one instruction (sm_100+ packed f32x2).
+// Two fp32 FMAs in one instruction (sm_100+ packed f32x2); operands are packed
+// inside the asm so no local ever needs an address.
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-  uint64_t ra = *reinterpret_cast<uint64_t *>(&a);
-  uint64_t rb = *reinterpret_cast<uint64_t *>(&b);
-  uint64_t rc = *reinterpret_cast<uint64_t *>(&c);
-  uint64_t rd;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
-  return *reinterpret_cast<float2 *>(&rd);
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
+// Two fp32 adds in one instruction (sm_100+ packed f32x2).
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+// max of three floats in one instruction (sm_100+).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 __device__ __forceinline__ float2 h2_to_f2(uint32_t h) {

@@ -63,18 +63,11 @@ __device__ __forceinline__ void it_token(UnitIt &it, int i, const DecView &v) {
   it.L = min(max(L, 0), v.cap);
 }
 
-// Unit u -> (i, g, kb).  Units of token i occupy [Hkv*off[i], Hkv*off[i+1]).
-__device__ __forceinline__ void it_seek(UnitIt &it, int u, const DecView &v) {
-  int lo = 0, hi = v.n_dec - 1;  // largest i with Hkv*off[i] <= u
-  while (lo < hi) {
-    int mid = (lo + hi + 1) >> 1;
-    if (v.Hkv * v.tok_unit_off[mid] <= u) lo = mid; else hi = mid - 1;
-  }
-  it_token(it, lo, v);
-  while (it.units == 0) it_token(it, it.i + 1, v);
-  int r = u - v.Hkv * v.tok_unit_off[it.i];
-  it.g = r / it.units;
-  it.kb = r - it.g * it.units;
+// Iterator at the CTA's first unit, as placed by the planner: (i, g, kb).
+__device__ __forceinline__ void it_start(UnitIt &it, int4 st, const DecView &v) {
+  it_token(it, st.x, v);
+  it.g = st.y;
+  it.kb = st.z;
 }
 
 __device__ __forceinline__ void it_next(UnitIt &it, const DecView &v) {
@@ -161,8 +154,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(AttnArgs a) {
   __syncwarp();
 
   // producer state (lane 0 of every warp walks the same unit sequence)
+  const int4 start = reinterpret_cast<const int4 *>(a.ws + a.lay.dec_start)[c];
   UnitIt pit;
-  it_seek(pit, u0, v);
+  it_start(pit, start, v);
   int issued = 0;      // units whose copies lane 0 has started
   int k_dead = n;      // first unit whose wait gave up
   auto issue = [&](int k) {
@@ -186,7 +180,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(AttnArgs a) {
   }
 
   UnitIt cit;
-  it_seek(cit, u0, v);
+  it_start(cit, start, v);
   int seg_i = -1, seg_g = -1, seg_begin = 0, seg_units = 0, seg_tok = 0;
   float qf[G][NCH][8];
   float m_run[G], l_run[G];

@@ -5,6 +5,13 @@
 // heads share every K/V tile the CTA loads (GQA grouping), so one 128-key block
 // of K and of V is fetched once for 2 x 128 query rows.
 //
+// Scheduling is stream-K: the (item, 128-key block) units of the ubatch are
+// laid end to end and cut into C equal contiguous ranges, one per CTA, so
+// every SM gets the same tensor work whatever the item count.  An item cut by
+// a range boundary is computed in parts; each part leaves (m, l, unnormalised
+// O) per row, and the CTA that finishes the item's last part combines them
+// (an arrival counter decides who is last; nobody waits).
+//
 // Warp roles (384 threads = 3 warpgroups, one CTA per SM, persistent over items):
 //   warps 0-3  softmax of query tile 0 (thread = query row = TMEM lane)
 //   warps 4-7  softmax of query tile 1
@@ -33,7 +40,7 @@ namespace pa {
 
 constexpr int kPfThreads = 384;
 constexpr int kRegsSoftmax = 192;   // per thread, warpgroups 0 and 1
-constexpr int kRegsOther = 104;     // per thread, warpgroup 2
+constexpr int kRegsOther = 120;     // per thread, warpgroup 2
 // registers the split needs from the launch; checked on the host before launching
 constexpr int kRegsSplitTotal = 2 * 128 * kRegsSoftmax + 128 * kRegsOther;
 constexpr int kPfStages = 2;
@@ -80,31 +87,69 @@ __device__ __forceinline__ bool pf_wait(uint64_t *bar, uint32_t parity, int *err
   }
 }
 
-struct Item {
-  int tile_start, n_tok, nkb, max_kv, g, h0, h1;
+// One contiguous piece of work of a CTA: key blocks [kb_b, kb_e) of one item.
+struct Seg {
+  int tile, j;              // tile index, item within the tile
+  int kb_b, kb_e;           // key-block range of this piece
+  int nkb, max_kv;          // whole item: key blocks, longest kv_len of the tile
+  int tile_start, n_tok;    // tokens of the tile
+  int g, h0, h1;            // KV head, query heads of the pair
+  long long w, w_end;       // unit position of this piece, end of the CTA's range
+  long long item_start;     // unit index of the item's key block 0
 };
 
-__device__ __forceinline__ Item decode_item(int item, const int4 *tiles, int Hkv, int G) {
-  const int NP = G >= 2 ? G / 2 : 1;
-  Item it;
-  int tile = item / (Hkv * NP);
-  int rem = item - tile * Hkv * NP;
-  it.g = rem / NP;
-  int pair = rem - it.g * NP;
-  int4 tl = tiles[tile];
-  it.tile_start = tl.x;
-  it.n_tok = tl.y;
-  it.nkb = tl.z;
-  it.max_kv = tl.w;
-  it.h0 = G >= 2 ? it.g * G + 2 * pair : it.g;
-  it.h1 = it.h0 + 1;
-  return it;
+struct SegCtx {
+  const int4 *tiles;
+  const int *tile_off;
+  int Hkv, NP, G, items_per_tile;
+};
+
+__device__ __forceinline__ void seg_load(Seg &s, const SegCtx &x) {
+  int4 tl = x.tiles[s.tile];
+  s.tile_start = tl.x;
+  s.n_tok = tl.y;
+  s.nkb = tl.z;
+  s.max_kv = tl.w;
+  s.g = s.j / x.NP;
+  const int pair = s.j - s.g * x.NP;
+  s.h0 = x.G >= 2 ? s.g * x.G + 2 * pair : s.g;
+  s.h1 = s.h0 + 1;
+  s.item_start = (long long)x.tile_off[s.tile] + (long long)s.j * s.nkb;
+}
+
+__device__ __forceinline__ bool seg_first(Seg &s, const SegCtx &x, int4 start, long long w0,
+                                          long long w1) {
+  if (w0 >= w1) return false;
+  s.tile = start.x;
+  s.j = start.y;
+  seg_load(s, x);
+  s.w = w0;
+  s.w_end = w1;
+  s.kb_b = start.z;
+  s.kb_e = (int)min((long long)s.nkb, s.kb_b + (w1 - w0));
+  return true;
+}
+
+__device__ __forceinline__ bool seg_next(Seg &s, const SegCtx &x) {
+  s.w += s.kb_e - s.kb_b;
+  if (s.w >= s.w_end) return false;
+  if (++s.j == x.items_per_tile) {  // next tile that has keys (there is one: w < w_end <= W)
+    s.j = 0;
+    do { ++s.tile; } while (x.tiles[s.tile].z == 0);
+  }
+  seg_load(s, x);
+  s.kb_b = 0;
+  s.kb_e = (int)min((long long)s.nkb, s.w_end - s.w);
+  return true;
 }
 
 template <int D>
 __global__ void __launch_bounds__(kPfThreads, 1)
 k_prefill(AttnArgs a, const __grid_constant__ PrefillMaps maps) {
   using Cfg = PfCfg<D>;
+  // row record of a split part: O[D] | m | l | pad -- a multiple of 16 bytes so that
+  // every row's record starts 16-byte aligned for float4 access
+  constexpr int kPartStride = D + 4;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
   unsigned char *smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
@@ -116,10 +161,28 @@ k_prefill(AttnArgs a, const __grid_constant__ PrefillMaps maps) {
   const int G = a.Hq / a.Hkv;
   const int NQ = G >= 2 ? 2 : 1;
   const int NP = G >= 2 ? G / 2 : 1;
-  const int n_items = hdr->n_tiles * a.Hkv * NP;
-  if ((int)blockIdx.x >= n_items) return;
-
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int C = hdr->C;
+  const int c = blockIdx.x;
+  if (c >= C) return;
+  // tiles whose tokens all have kv_len 0 own no work unit: their rows are zero
+  for (int t = c; t < hdr->n_tiles; t += C) {
+    const int4 tl = tiles[t];
+    if (tl.z != 0) continue;
+    for (int x = tid; x < tl.y * a.Hq * (D / 8); x += blockDim.x)
+      reinterpret_cast<uint4 *>(a.out + (size_t)tl.x * a.Hq * D)[x] = make_uint4(0, 0, 0, 0);
+  }
+  const long long W = hdr->pf_work;
+  const long long w0 = (long long)c * W / C, w1 = (long long)(c + 1) * W / C;
+  if (w0 >= w1) return;
+  SegCtx sx;
+  sx.tiles = tiles;
+  sx.tile_off = reinterpret_cast<const int *>(a.ws + a.lay.tile_off);
+  sx.Hkv = a.Hkv;
+  sx.NP = NP;
+  sx.G = G;
+  sx.items_per_tile = a.Hkv * NP;
+  const int4 start = reinterpret_cast<const int4 *>(a.ws + a.lay.pf_start)[c];
   if (tid == 0) {
     mbar_init(&bars->q_full, 1);
     mbar_init(&bars->q_empty, 1);
@@ -163,9 +226,8 @@ k_prefill(AttnArgs a, const __grid_constant__ PrefillMaps maps) {
       int nitem = 0;
       const int pages_per_block = KB / a.P;
       const int oob_row = a.num_pages * a.Hkv * a.P;  // first row past the pool: zero fill
-      for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-        Item w = decode_item(item, tiles, a.Hkv, G);
-        if (w.nkb == 0) continue;
+      Seg w;
+      for (bool more = seg_first(w, sx, start, w0, w1); more; more = seg_next(w, sx)) {
         if (nitem > 0 && !pf_wait(&bars->q_empty, (nitem - 1) & 1, err, abort)) break;
         mbar_arrive_expect_tx(&bars->q_full, NQ * Cfg::kTile);
         for (int hf = 0; hf < Cfg::kHalves; ++hf) {
@@ -177,7 +239,7 @@ k_prefill(AttnArgs a, const __grid_constant__ PrefillMaps maps) {
         }
         const int32_t *row = a.tpt + (size_t)w.tile_start * a.max_pages;
         bool ok = true;
-        for (int kb = 0; kb < w.nkb && ok; ++kb, ++it) {
+        for (int kb = w.kb_b; kb < w.kb_e && ok; ++kb, ++it) {
           const int st = it % kPfStages;
           const uint32_t ph = (it / kPfStages) & 1u;
           const int keys = min(KB, w.max_kv - kb * KB);
@@ -239,9 +301,9 @@ k_prefill(AttnArgs a, const __grid_constant__ PrefillMaps maps) {
     const bool leader = lane == 0;
     uint32_t it = 0, sc = 0;
     int nitem = 0;
-    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-      Item w = decode_item(item, tiles, a.Hkv, G);
-      if (w.nkb == 0) continue;
+    Seg w;
+    for (bool more = seg_first(w, sx, start, w0, w1); more; more = seg_next(w, sx)) {
+      const int nseg = w.kb_e - w.kb_b;
       bool ok = pf_wait(&bars->q_full, nitem & 1, err, abort);
       const int st0 = it % kPfStages;
       ok = ok && pf_wait(&bars->k_full[st0], (it / kPfStages) & 1u, err, abort);
@@ -257,13 +319,14 @@ k_prefill(AttnArgs a, const __grid_constant__ PrefillMaps maps) {
         tc::commit(&bars->k_empty[st0]);
       }
       __syncwarp();
-      for (int kb = 0; kb < w.nkb; ++kb) {
-        const uint32_t cur = it + kb;
+      for (int kk = 0; kk < nseg; ++kk) {
+        const int kb = w.kb_b + kk;  // absolute key block
+        const uint32_t cur = it + kk;
         const int st = cur % kPfStages;
-        const bool last = kb + 1 == w.nkb;
+        const bool last = kk + 1 == nseg;
         if (!pf_wait(&bars->v_full[st], (cur / kPfStages) & 1u, err, abort)) { ok = false; break; }
         const int nvalid = w.max_kv - kb * KB;
-        if (last && nvalid < KB) {
+        if (kb + 1 == w.nkb && nvalid < KB) {
           // zero V rows nvalid..127 in each 64-column box (rows are 128 B, whole rows
           // are zeroed so the swizzle inside a row does not matter)
           for (int hf = 0; hf < Cfg::kHalves; ++hf) {
@@ -275,14 +338,14 @@ k_prefill(AttnArgs a, const __grid_constant__ PrefillMaps maps) {
           fence_proxy_async();
         }
         __syncwarp();
-        if (!pf_wait(&bars->p_full[0], (sc + kb) & 1u, err, abort)) { ok = false; break; }
-        if (kb == 0 && nitem > 0 && !pf_wait(&bars->o_empty[0], (nitem - 1) & 1, err, abort)) {
+        if (!pf_wait(&bars->p_full[0], (sc + kk) & 1u, err, abort)) { ok = false; break; }
+        if (kk == 0 && nitem > 0 && !pf_wait(&bars->o_empty[0], (nitem - 1) & 1, err, abort)) {
           ok = false;
           break;
         }
         tc::fence_after_sync();
         if (leader) {
-          issue_PV(0, st, kb > 0);
+          issue_PV(0, st, kk > 0);
           if (last) tc::commit(&bars->o_full[0]);
         }
         __syncwarp();
@@ -299,14 +362,14 @@ k_prefill(AttnArgs a, const __grid_constant__ PrefillMaps maps) {
           __syncwarp();
         }
         if (NQ == 2) {
-          if (!pf_wait(&bars->p_full[1], (sc + kb) & 1u, err, abort)) { ok = false; break; }
-          if (kb == 0 && nitem > 0 && !pf_wait(&bars->o_empty[1], (nitem - 1) & 1, err, abort)) {
+          if (!pf_wait(&bars->p_full[1], (sc + kk) & 1u, err, abort)) { ok = false; break; }
+          if (kk == 0 && nitem > 0 && !pf_wait(&bars->o_empty[1], (nitem - 1) & 1, err, abort)) {
             ok = false;
             break;
           }
           tc::fence_after_sync();
           if (leader) {
-            issue_PV(1, st, kb > 0);
+            issue_PV(1, st, kk > 0);
             if (last) tc::commit(&bars->o_full[1]);
           }
         }
@@ -325,8 +388,8 @@ k_prefill(AttnArgs a, const __grid_constant__ PrefillMaps maps) {
       if (!ok) break;
       if (leader) tc::commit(&bars->q_empty);
       __syncwarp();
-      it += w.nkb;
-      sc += w.nkb;
+      it += nseg;
+      sc += nseg;
       ++nitem;
     }
    }
@@ -342,62 +405,86 @@ k_prefill(AttnArgs a, const __grid_constant__ PrefillMaps maps) {
     if (wg < NQ) {
       uint32_t sc = 0;
       int nitem = 0;
-      for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-        Item w = decode_item(item, tiles, a.Hkv, G);
+      float *parts = reinterpret_cast<float *>(a.ws + a.lay.partials);
+      int *cnt = reinterpret_cast<int *>(a.ws + a.lay.pf_cnt);
+      Seg w;
+      for (bool more = seg_first(w, sx, start, w0, w1); more; more = seg_next(w, sx)) {
         const int h = wg ? w.h1 : w.h0;
         const int tok = w.tile_start + row;
         const bool valid = row < w.n_tok;
         const int L = valid ? min(max(a.kv[tok], 0), cap) : 0;
         uint4 *orow = reinterpret_cast<uint4 *>(a.out + ((size_t)tok * a.Hq + h) * D);
-        if (w.nkb == 0) {
-          if (valid)
-            for (int x = 0; x < D / 8; ++x) orow[x] = make_uint4(0, 0, 0, 0);
-          continue;
-        }
+        const int nseg = w.kb_e - w.kb_b;
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
-        for (int kb = 0; kb < w.nkb; ++kb) {
-          if (!pf_wait(&bars->s_full[wg], (sc + kb) & 1u, err, abort)) { ok = false; break; }
+        for (int kk = 0; kk < nseg; ++kk) {
+          const int kb = w.kb_b + kk;
+          if (!pf_wait(&bars->s_full[wg], (sc + kk) & 1u, err, abort)) { ok = false; break; }
           tc::fence_after_sync();
-          uint32_t s[4][32];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) tc::ld32(tS + c * 32, s[c]);
-          tc::wait_ld();
-          const int nv = min(max(L - kb * KB, 0), KB);
+          const int nv = min(max(L - kb * KB, 0), KB);  // valid keys of this row here
+          const bool wfull = __all_sync(0xffffffffu, nv == KB);
+          // pass 1: row max of the raw scores over the valid keys, 64 columns at a time
+          // (scale > 0 commutes with max).  Masked scores become -inf by select, so
+          // NaN cells never propagate.
           float mx = -INFINITY;
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t t0[32], t1[32];
+            tc::ld32(tS + 64 * hh, t0);
+            tc::ld32(tS + 64 * hh + 32, t1);
+            tc::wait_ld();
+            if (wfull) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float x = (c * 32 + j < nv) ? __uint_as_float(s[c][j]) * a.scale_log2
-                                                 : -INFINITY;
-              s[c][j] = __float_as_uint(x);
-              mx = fmaxf(mx, x);
+              for (int j = 0; j < 32; ++j)
+                mx = fmax3(mx, __uint_as_float(t0[j]), __uint_as_float(t1[j]));
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const int k0 = 64 * hh + j;
+                mx = fmax3(mx, k0 < nv ? __uint_as_float(t0[j]) : -INFINITY,
+                           k0 + 32 < nv ? __uint_as_float(t1[j]) : -INFINITY);
+              }
             }
-          const float m_new = fmaxf(m_run, mx);
+          }
+          const float m_new = fmaxf(m_run, mx * a.scale_log2);
           const bool need = m_new > m_run + kRescaleThreshold;
           float alpha = 1.f;
           if (need) {
             alpha = exp2_approx(m_run - m_new);
             m_run = m_new;
           }
+          // pass 2: p = 2^(s * scale_log2 - m), one packed FMA per pair, then ex2; a row
+          // with no valid key yet uses m = 0 so that its -inf scores give exactly 0.
+          // P (f16) goes to the first 64 columns of S: half hh lands in columns
+          // [32hh, 32hh+32), below the columns half hh+1 still has to read.
+          const float m_use = m_run == -INFINITY ? 0.f : m_run;
+          const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
+          const float2 nm2 = make_float2(-m_use, -m_use);
           float rs = 0.f;
-          uint32_t pk[2][32];
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t t[64];
+            tc::ld32(tS + 64 * hh, *reinterpret_cast<uint32_t(*)[32]>(t));
+            tc::ld32(tS + 64 * hh + 32, *reinterpret_cast<uint32_t(*)[32]>(t + 32));
+            tc::wait_ld();
+            uint32_t pk[32];
 #pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              const float x0 = __uint_as_float(s[c][j]), x1 = __uint_as_float(s[c][j + 1]);
-              const float p0 = x0 == -INFINITY ? 0.f : exp2_approx(x0 - m_run);
-              const float p1 = x1 == -INFINITY ? 0.f : exp2_approx(x1 - m_run);
+            for (int j = 0; j < 64; j += 2) {
+              float2 x = ffma2(make_float2(__uint_as_float(t[j]), __uint_as_float(t[j + 1])),
+                               sc2, nm2);
+              if (!wfull) {
+                x.x = 64 * hh + j < nv ? x.x : -INFINITY;
+                x.y = 64 * hh + j + 1 < nv ? x.y : -INFINITY;
+              }
+              const float p0 = exp2_approx(x.x), p1 = exp2_approx(x.y);
               rs += p0 + p1;
               __half2 hp = __floats2half2_rn(p0, p1);
-              pk[c >> 1][(c & 1) * 16 + (j >> 1)] = *reinterpret_cast<uint32_t *>(&hp);
+              pk[j >> 1] = *reinterpret_cast<uint32_t *>(&hp);
             }
+            tc::st32(tS + 32 * hh, pk);
+          }
           l_run = l_run * alpha + rs;
-          tc::st32(tS, pk[0]);
-          tc::st32(tS + 32, pk[1]);
-          if (kb > 0 && __any_sync(0xffffffffu, need)) {
+          if (kk > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
               uint32_t o[32];
@@ -415,29 +502,119 @@ k_prefill(AttnArgs a, const __grid_constant__ PrefillMaps maps) {
         if (!ok) break;
         if (!pf_wait(&bars->o_full[wg], nitem & 1, err, abort)) break;
         tc::fence_after_sync();
-        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        if (w.kb_b == 0 && w.kb_e == w.nkb) {
+          // the whole item: normalise and store f16
+          const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tc::ld32(tO + c * 32, o);
-          tc::wait_ld();
-          if (valid) {
+          for (int ch = 0; ch < D / 32; ++ch) {
+            uint32_t o[32];
+            tc::ld32(tO + ch * 32, o);
+            tc::wait_ld();
+            if (valid) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint32_t hw[4];
+              for (int q = 0; q < 4; ++q) {
+                uint32_t hw[4];
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                __half2 hv = __floats2half2_rn(__uint_as_float(o[q * 8 + 2 * e]) * inv,
-                                               __uint_as_float(o[q * 8 + 2 * e + 1]) * inv);
-                hw[e] = *reinterpret_cast<uint32_t *>(&hv);
+                for (int e = 0; e < 4; ++e) {
+                  __half2 hv = __floats2half2_rn(__uint_as_float(o[q * 8 + 2 * e]) * inv,
+                                                 __uint_as_float(o[q * 8 + 2 * e + 1]) * inv);
+                  hw[e] = *reinterpret_cast<uint32_t *>(&hv);
+                }
+                orow[ch * 4 + q] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
               }
-              orow[c * 4 + q] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
             }
           }
+          tc::fence_before_sync();
+          mbar_arrive(&bars->o_empty[wg]);
+        } else {
+          // one part of a split item: leave (O unnormalised, m, l) in this CTA's slot
+          const bool first_seg = w.item_start <= w0;
+          const int my_slot = 2 * c + (first_seg ? 0 : 1);
+          float *rec = parts + (((size_t)my_slot * 2 + wg) * 128 + row) * kPartStride;
+#pragma unroll
+          for (int ch = 0; ch < D / 32; ++ch) {
+            uint32_t o[32];
+            tc::ld32(tO + ch * 32, o);
+            tc::wait_ld();
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              reinterpret_cast<float4 *>(rec + ch * 32)[q] =
+                  make_float4(__uint_as_float(o[4 * q]), __uint_as_float(o[4 * q + 1]),
+                              __uint_as_float(o[4 * q + 2]), __uint_as_float(o[4 * q + 3]));
+          }
+          rec[D] = m_run;
+          rec[D + 1] = l_run;
+          tc::fence_before_sync();
+          mbar_arrive(&bars->o_empty[wg]);
+          // count the parts that have landed; the last one combines (no waiting)
+          const long long item_end = w.item_start + w.nkb;
+          const int c1 = cta_of_unit(w.item_start, W, C), c2 = cta_of_unit(item_end - 1, W, C);
+          int n_parts = 0;
+          for (int cc = c1; cc <= c2; ++cc) n_parts += cta_has_units(cc, W, C) ? 1 : 0;
+          // one counter per (item, warpgroup, warp): a warp's 32 rows only need the same
+          // 32 rows of the other parts, so warps decide independently (no cross-warp wait)
+          int *my_cnt = &cnt[((w.tile * sx.items_per_tile + w.j) * 2 + wg) * 4 + wl];
+          __threadfence();
+          __syncwarp();
+          int old = 0;
+          if (lane == 0) old = atomicAdd(my_cnt, 1);
+          old = __shfl_sync(0xffffffffu, old, 0);
+          if (old == n_parts - 1) {
+            __threadfence();
+            // the other parts were written by other SMs: read them past L1 (ld.global.cg)
+            float M = -INFINITY;
+            for (int cc = c1; cc <= c2; ++cc) {
+              if (!cta_has_units(cc, W, C)) continue;
+              const int sl = 2 * cc + (w.item_start <= (long long)cc * W / C ? 0 : 1);
+              M = fmaxf(M, __ldcg(parts + (((size_t)sl * 2 + wg) * 128 + row) * kPartStride + D));
+            }
+            float Ls = 0.f;
+            for (int cc = c1; cc <= c2; ++cc) {
+              if (!cta_has_units(cc, W, C)) continue;
+              const int sl = 2 * cc + (w.item_start <= (long long)cc * W / C ? 0 : 1);
+              const float *r = parts + (((size_t)sl * 2 + wg) * 128 + row) * kPartStride;
+              const float m_p = __ldcg(r + D);
+              Ls += (m_p == -INFINITY) ? 0.f : __ldcg(r + D + 1) * exp2_approx(m_p - M);
+            }
+            const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+#pragma unroll 1
+            for (int ch = 0; ch < D / 32; ++ch) {
+              float acc[32];
+#pragma unroll
+              for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+              for (int cc = c1; cc <= c2; ++cc) {
+                if (!cta_has_units(cc, W, C)) continue;
+                const int sl = 2 * cc + (w.item_start <= (long long)cc * W / C ? 0 : 1);
+                const float *r = parts + (((size_t)sl * 2 + wg) * 128 + row) * kPartStride;
+                const float m_p = __ldcg(r + D);
+                const float f = (m_p == -INFINITY) ? 0.f : exp2_approx(m_p - M);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                  const float4 v4 = __ldcg(reinterpret_cast<const float4 *>(r + ch * 32) + q);
+                  acc[4 * q] += f * v4.x;
+                  acc[4 * q + 1] += f * v4.y;
+                  acc[4 * q + 2] += f * v4.z;
+                  acc[4 * q + 3] += f * v4.w;
+                }
+              }
+              if (valid) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                  uint32_t hw[4];
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    __half2 hv = __floats2half2_rn(acc[q * 8 + 2 * e] * inv,
+                                                   acc[q * 8 + 2 * e + 1] * inv);
+                    hw[e] = *reinterpret_cast<uint32_t *>(&hv);
+                  }
+                  orow[ch * 4 + q] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                }
+              }
+            }
+            if (lane == 0) *my_cnt = 0;  // ready for the next run of this plan
+          }
         }
-        tc::fence_before_sync();
-        mbar_arrive(&bars->o_empty[wg]);
-        sc += w.nkb;
+        sc += nseg;
         ++nitem;
       }
     }

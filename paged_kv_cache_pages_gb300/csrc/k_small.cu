@@ -94,7 +94,30 @@ __global__ void k_validate(const int32_t *__restrict__ tpt, int max_pages,
 }
 
 // ---------------------------------------------------------------------------
-// Planner (one CTA of 1024 threads).
+// Planner, part 1 (many CTAs): flags[t] = 1 if token t starts a run, i.e. its
+// page-table row differs from row t-1 in any byte.  One warp per token.
+// ---------------------------------------------------------------------------
+__global__ void k_plan_mark(const int32_t *__restrict__ tpt, int max_pages, int T,
+                            unsigned char *ws, WsLayout lay) {
+  int *flags = reinterpret_cast<int *>(ws + lay.flags);
+  int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  int lane = threadIdx.x & 31;
+  int nwarps = (gridDim.x * blockDim.x) >> 5;
+  for (int t = warp; t < T; t += nwarps) {
+    bool d = (t == 0);
+    if (!d) {
+      const int32_t *a = tpt + (size_t)t * max_pages;
+      const int32_t *b = a - max_pages;
+      bool x = false;
+      for (int i = lane; i < max_pages; i += 32) x |= (a[i] != b[i]);
+      d = __any_sync(0xffffffffu, x);
+    }
+    if (lane == 0) flags[t] = d ? 1 : 0;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Planner, part 2 (one CTA of 1024 threads).
 // ---------------------------------------------------------------------------
 constexpr int kPlanThreads = 1024;
 
@@ -126,9 +149,19 @@ __device__ int block_excl_scan(int v, int *total, int *sh) {
   return warp_prefix + x - v;
 }
 
+// Largest i in [0, n] with off[i] * scale <= u (off non-decreasing, off[0] = 0).
+__device__ __forceinline__ int upper_index(const int *off, int n, long long u, long long scale) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if ((long long)off[mid] * scale <= u) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
 __global__ void __launch_bounds__(kPlanThreads, 1)
 k_plan(const int32_t *__restrict__ tpt, int max_pages, const int32_t *__restrict__ kv, int T,
-       int P, int Hkv, int min_run, unsigned char *ws, WsLayout lay) {
+       int P, int Hkv, int NP, int min_run, int C, unsigned char *ws, WsLayout lay) {
   __shared__ int sh[32];
   WsHeader *hdr = reinterpret_cast<WsHeader *>(ws);
   int4 *tiles = reinterpret_cast<int4 *>(ws + lay.tiles);
@@ -136,29 +169,16 @@ k_plan(const int32_t *__restrict__ tpt, int max_pages, const int32_t *__restrict
   int *tok_unit_off = reinterpret_cast<int *>(ws + lay.tok_unit_off);
   int *flags = reinterpret_cast<int *>(ws + lay.flags);
   int *runs = reinterpret_cast<int *>(ws + lay.runs);
+  int *tile_off = reinterpret_cast<int *>(ws + lay.tile_off);
+  int4 *dec_start = reinterpret_cast<int4 *>(ws + lay.dec_start);
+  int4 *pf_start = reinterpret_cast<int4 *>(ws + lay.pf_start);
+  int *pf_cnt = reinterpret_cast<int *>(ws + lay.pf_cnt);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int cap = max_pages * P;
 
-  if (tid == 0) {
-    hdr->err = 0;
-    hdr->tile_next = 0;
-    hdr->tile_done = 0;
-  }
-  // 1. run starts: token t starts a run unless its row equals row t-1 byte for byte
-  for (int t = warp; t < T; t += kPlanThreads / 32) {
-    bool diff = (t == 0);
-    if (!diff) {
-      const int32_t *a = tpt + (size_t)t * max_pages;
-      const int32_t *b = a - max_pages;
-      bool d = false;
-      for (int i = lane; i < max_pages; i += 32) d |= (a[i] != b[i]);
-      diff = __any_sync(0xffffffffu, d);
-    }
-    if (lane == 0) flags[t] = diff ? 1 : 0;
-  }
-  __syncthreads();
+  if (tid == 0) hdr->err = 0;
 
-  // 2. run ids by an inclusive scan of the start flags; runs[r] = first token of run r
+  // 1. run ids by a scan of the start flags; runs[r] = first token of run r
   int n_runs = 0;
   for (int c0 = 0; c0 < T; c0 += kPlanThreads) {
     int t = c0 + tid;
@@ -171,7 +191,7 @@ k_plan(const int32_t *__restrict__ tpt, int max_pages, const int32_t *__restrict
   if (tid == 0) runs[n_runs] = T;
   __syncthreads();
 
-  // 3. runs of >= min_run tokens become tiles of <= 128 tokens (near-equal
+  // 2. runs of >= min_run tokens become tiles of <= 128 tokens (near-equal
   //    split); shorter runs become decode tokens.
   int tile_base = 0, dec_base = 0;
   for (int c0 = 0; c0 < n_runs; c0 += kPlanThreads) {
@@ -182,19 +202,24 @@ k_plan(const int32_t *__restrict__ tpt, int max_pages, const int32_t *__restrict
     int n_tiles = prefill_run ? (len + KB - 1) / KB : 0;
     int n_dec = (r < n_runs && !prefill_run) ? len : 0;
     int tot_tiles, tot_dec;
-    int tile_off = block_excl_scan(n_tiles, &tot_tiles, sh) + tile_base;
+    int tile_off0 = block_excl_scan(n_tiles, &tot_tiles, sh) + tile_base;
     int dec_off = block_excl_scan(n_dec, &tot_dec, sh) + dec_base;
     for (int i = 0; i < n_tiles; ++i) {
       int b0 = a + (int)((int64_t)len * i / n_tiles);
       int b1 = a + (int)((int64_t)len * (i + 1) / n_tiles);
-      tiles[tile_off + i] = make_int4(b0, b1 - b0, 0, 0);
+      tiles[tile_off0 + i] = make_int4(b0, b1 - b0, 0, 0);
     }
     for (int i = 0; i < n_dec; ++i) dec_tok[dec_off + i] = a + i;
     tile_base += tot_tiles;
     dec_base += tot_dec;
   }
   __syncthreads();
-  // 4. key blocks of each tile: ceil(max kv_len over its tokens / 128); one warp per tile
+
+  // arrival counters of this plan's prefill items start at zero (the combining
+  // part resets its counter after use, so later runs of the plan find zeros too)
+  for (int i = tid; i < tile_base * Hkv * NP * 8; i += kPlanThreads) pf_cnt[i] = 0;
+
+  // 3. key blocks of each tile: ceil(max kv_len over its tokens / 128); one warp per tile
   for (int i = warp; i < tile_base; i += kPlanThreads / 32) {
     int4 tl = tiles[i];
     int mx = 0;
@@ -212,8 +237,22 @@ k_plan(const int32_t *__restrict__ tpt, int max_pages, const int32_t *__restrict
       tiles[i].w = mx;
     }
   }
+  __syncthreads();
+
+  // 4. prefill work prefix over tiles: each tile holds Hkv * NP items of n_kblocks units
+  int work_base = 0;
+  for (int c0 = 0; c0 < tile_base; c0 += kPlanThreads) {
+    int i = c0 + tid;
+    int wk = i < tile_base ? tiles[i].z * Hkv * NP : 0;
+    int tot;
+    int off = block_excl_scan(wk, &tot, sh) + work_base;
+    if (i < tile_base) tile_off[i] = off;
+    work_base += tot;
+  }
+  if (tid == 0) tile_off[tile_base] = work_base;
+
+  // 5. decode units: 128-key blocks per decode token, prefix-summed
   int unit_base = 0;
-  // 3. decode units: 128-key blocks per decode token, prefix-summed
   for (int c0 = 0; c0 < dec_base; c0 += kPlanThreads) {
     int i = c0 + tid;
     int units = 0;
@@ -226,13 +265,43 @@ k_plan(const int32_t *__restrict__ tpt, int max_pages, const int32_t *__restrict
     int off = block_excl_scan(units, &tot, sh) + unit_base;
     if (i < dec_base) tok_unit_off[i] = off;
     unit_base += tot;
-    __syncthreads();
+  }
+  if (tid == 0) tok_unit_off[dec_base] = unit_base;
+  __syncthreads();
+
+  // 6. where each of the C CTAs starts in the decode and in the prefill work
+  const long long U = (long long)unit_base * Hkv, W = work_base;
+  for (int c = tid; c < C; c += kPlanThreads) {
+    if (U > 0) {
+      long long u = (long long)c * U / C;
+      int i = upper_index(tok_unit_off, dec_base, u, Hkv);
+      if (i >= dec_base) i = dec_base - 1;
+      int units = tok_unit_off[i + 1] - tok_unit_off[i];
+      while (units == 0 && i + 1 < dec_base) {  // tokens without keys own no unit
+        ++i;
+        units = tok_unit_off[i + 1] - tok_unit_off[i];
+      }
+      long long r = u - (long long)Hkv * tok_unit_off[i];
+      int g = units > 0 ? (int)(r / units) : 0;
+      dec_start[c] = make_int4(i, g, units > 0 ? (int)(r - (long long)g * units) : 0, 0);
+    }
+    if (W > 0) {
+      long long w = (long long)c * W / C;
+      int t = upper_index(tile_off, tile_base, w, 1);
+      if (t >= tile_base) t = tile_base - 1;
+      while (tiles[t].z == 0 && t + 1 < tile_base) ++t;
+      int nkb = tiles[t].z;
+      long long r = w - tile_off[t];
+      int j = nkb > 0 ? (int)(r / nkb) : 0;
+      pf_start[c] = make_int4(t, j, nkb > 0 ? (int)(r - (long long)j * nkb) : 0, 0);
+    }
   }
   if (tid == 0) {
-    tok_unit_off[dec_base] = unit_base;
     hdr->n_tiles = tile_base;
     hdr->n_dec = dec_base;
-    hdr->n_units = unit_base * Hkv;
+    hdr->n_units = (int)U;
+    hdr->pf_work = work_base;
+    hdr->C = C;
     hdr->T = T;
     hdr->Hkv = Hkv;
     hdr->P = P;

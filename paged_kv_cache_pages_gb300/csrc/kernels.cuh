@@ -12,8 +12,10 @@ __global__ void k_append(const uint4 *k, const uint4 *v, const int64_t *slot, in
                          uint4 *vp, int num_pages, int Hkv, int P, int chunks_per_row, int *err);
 __global__ void k_validate(const int32_t *tpt, int max_pages, const int32_t *kv, int T, int P,
                            int num_pages, int *err);
+__global__ void k_plan_mark(const int32_t *tpt, int max_pages, int T, unsigned char *ws,
+                            WsLayout lay);
 __global__ void k_plan(const int32_t *tpt, int max_pages, const int32_t *kv, int T, int P, int Hkv,
-                       int min_run, unsigned char *ws, WsLayout lay);
+                       int NP, int min_run, int C, unsigned char *ws, WsLayout lay);
 
 // Arguments of the attention kernels (passed by value).
 struct AttnArgs {

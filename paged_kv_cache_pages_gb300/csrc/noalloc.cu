@@ -24,7 +24,7 @@
 
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
+constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;  // 64 MiB
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];

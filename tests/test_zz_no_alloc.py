@@ -5,7 +5,7 @@ paged_attn_forward_noalloc serves callers that cannot allocate device memory
 latency-critical path).  It must give the same output as paged_attn_forward
 with an allocated workspace, on two calls in a row (the second call finds the
 first call's leftovers in the shared scratch), and reject a ubatch too large
-for its fixed 16 MiB scratch.  This file is collected last on purpose.
+for its fixed 64 MiB scratch.  This file is collected last on purpose.
 """
 import ctypes
 
@@ -54,8 +54,8 @@ def test_noalloc_matches_forward_on_two_calls_in_a_row():
 def test_noalloc_rejects_ubatch_beyond_its_scratch():
     import paged_kv_cache_pages_gb300 as pa
     fn = _noalloc(pa.lib())
-    T, Hq, Hkv, d = 4096, 32, 8, 128
-    assert pa.workspace_size(T, Hq, Hkv, d) > (16 << 20)
+    T, Hq, Hkv, d = 8192, 32, 8, 128
+    assert pa.workspace_size(T, Hq, Hkv, d) > (64 << 20)
     q = torch.zeros((T, Hq, d), dtype=torch.float16, device="cuda")
     kp = torch.zeros((4, Hkv, 128, d), dtype=torch.float16, device="cuda")
     tpt = torch.zeros((T, 1), dtype=torch.int32, device="cuda")
