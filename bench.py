@@ -162,7 +162,7 @@ class PrefillBench:
         Tmax = max(d["T"] for d in self.ub)
         self.ws = pa.new_workspace(Tmax, wl.Hq, wl.Hkv, wl.d, dev)
         self.flops = sum(d["flops"] for d in self.ub)
-        self.launches_per_step = 7 * len(self.ub)   # expand, append, plan x2, prefill, decode, reduce
+        self.launches_per_step = 6 * len(self.ub)   # expand, append, plan x2, prefill, decode
 
     def _ubatch(self, d, ev=None):
         pa, wl = self.pa, self.wl
@@ -218,7 +218,7 @@ class DecodeBench:
         self.slot = t.empty(c.T, dtype=t.int64, device=dev)
         self.bytes_per_layer = float(c.seq_len.astype(np.int64).sum()) * c.Hkv * c.d * 2 * 2
         self.layers = layers
-        self.launches_per_step = 3 + 3 * layers   # expand, plan x2; per layer append, decode, reduce
+        self.launches_per_step = 3 + 2 * layers   # expand, plan x2; per layer append, decode
 
     def step(self, events=None):
         pa, c = self.pa, self.case
@@ -398,7 +398,7 @@ def run_ours(args):
                    "layers": db.layers, "kv_bytes_per_layer": db.bytes_per_layer,
                    "ms_per_step": round(d_step * 1e3, 3),
                    "gpu_launches": db.launches_per_step * args.steps,
-                   "roofline": {"bound": "hbm", "kernel": "k_decode + k_reduce",
+                   "roofline": {"bound": "hbm", "kernel": "k_decode",
                                 "achieved": round(d_ach, 1), "peak": hbm, "unit": "GB/s",
                                 "frac": round(d_ach / hbm, 4),
                                 "peak_source": f"{peak_src} hbm copy", "traffic": None}},

@@ -24,6 +24,7 @@ namespace pa {
 //   pf_start       int4 [C]      first prefill unit of each CTA: (tile, item in tile, kb, -)
 //   pf_cnt         int  [T * Hkv * NP * 2 * 4]  arrival counters of split prefill items,
 //                                  one per (item, softmax warpgroup, warp)
+//   dec_cnt        int  [T * Hkv]   arrival counters of decode segments split over CTAs
 //   partials       union of
 //                    decode split partials  float [(T*Hkv + C)][G][D + 2]
 //                    prefill split parts    float [2C][2][128][D + 4]  (16-byte rows)
@@ -46,6 +47,7 @@ constexpr int KB = 128;  // keys per block (decode unit and prefill key tile)
 
 struct WsLayout {
   size_t tiles, dec_tok, tok_unit_off, flags, runs, tile_off, dec_start, pf_start, pf_cnt;
+  size_t dec_cnt;
   size_t partials, total;
   int n_cnt;  // entries of pf_cnt
 };
@@ -68,6 +70,7 @@ __host__ __device__ inline WsLayout ws_layout(int T, int Hq, int Hkv, int D, int
   l.pf_start = o;     o = align_up(o + (size_t)C * 16, 256);
   l.n_cnt = (int)(Tm * Hkv * NP * 8);
   l.pf_cnt = o;       o = align_up(o + (size_t)l.n_cnt * 4, 256);
+  l.dec_cnt = o;      o = align_up(o + Tm * Hkv * 4, 256);
   l.partials = o;
   size_t dec_part = (Tm * Hkv + (size_t)C) * G * (D + 2) * 4;
   size_t pf_part = (size_t)2 * C * 2 * 128 * (D + 4) * 4;

@@ -173,6 +173,7 @@ k_plan(const int32_t *__restrict__ tpt, int max_pages, const int32_t *__restrict
   int4 *dec_start = reinterpret_cast<int4 *>(ws + lay.dec_start);
   int4 *pf_start = reinterpret_cast<int4 *>(ws + lay.pf_start);
   int *pf_cnt = reinterpret_cast<int *>(ws + lay.pf_cnt);
+  int *dec_cnt = reinterpret_cast<int *>(ws + lay.dec_cnt);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int cap = max_pages * P;
 
@@ -218,6 +219,7 @@ k_plan(const int32_t *__restrict__ tpt, int max_pages, const int32_t *__restrict
   // arrival counters of this plan's prefill items start at zero (the combining
   // part resets its counter after use, so later runs of the plan find zeros too)
   for (int i = tid; i < tile_base * Hkv * NP * 8; i += kPlanThreads) pf_cnt[i] = 0;
+  for (int i = tid; i < dec_base * Hkv; i += kPlanThreads) dec_cnt[i] = 0;
 
   // 3. key blocks of each tile: ceil(max kv_len over its tokens / 128); one warp per tile
   for (int i = warp; i < tile_base; i += kPlanThreads / 32) {
