@@ -186,8 +186,8 @@ int paged_attn_prefill(const uint16_t *q, const uint16_t *k_pages, const uint16_
   if (st != PA_OK || T == 0) return st;
   AttnArgs a = make_args(q, k_pages, v_pages, tok_page_table, max_pages, tok_kv_len, T, Hq, Hkv, P,
                          d, num_pages, scale, out, workspace);
-  PrefillMaps maps;
-  st = encode_prefill_maps(a, &maps);
+  AttnMaps maps;
+  st = encode_attn_maps(a, &maps);
   if (st != PA_OK) return st;
   return launch_status(launch_prefill(a, sm_count(), &maps, static_cast<cudaStream_t>(stream)));
 }
@@ -201,7 +201,10 @@ int paged_attn_decode(const uint16_t *q, const uint16_t *k_pages, const uint16_t
   if (st != PA_OK || T == 0) return st;
   AttnArgs a = make_args(q, k_pages, v_pages, tok_page_table, max_pages, tok_kv_len, T, Hq, Hkv, P,
                          d, num_pages, scale, out, workspace);
-  return launch_status(launch_decode(a, sm_count(), static_cast<cudaStream_t>(stream)));
+  AttnMaps maps;
+  st = encode_attn_maps(a, &maps);
+  if (st != PA_OK) return st;
+  return launch_status(launch_decode(a, sm_count(), &maps, static_cast<cudaStream_t>(stream)));
 }
 
 int paged_attn_run(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,

@@ -10,44 +10,52 @@
 // 核心架构 3, "Paged Attention V2", fused into one launch: an arrival counter
 // decides who combines, nobody waits).
 //
-// Inside a CTA (12 warps: 8 consumers, 1 producer, 1 combining warp, 2 idle; the consumers take
-// a larger register share with setmaxnreg) one producer thread streams, for every unit, the 128 K rows and
-// 128 V rows of the block (contiguous runs of the pool: one per page) and, at
-// the start of each (i, g), the G query rows, with 1-D bulk async copies into a
-// ring of stages; it runs up to NS units ahead of the consumers.  Eight
-// consumer warps each take 16 of the block's keys and compute the G = Hq/Hkv
-// query heads of the group against them (GQA grouping: every K/V byte is read
-// from HBM once per KV head).  Scores use fp32 FMAs; the softmax keeps a lazy
-// running max per head (one warp vote per block decides whether the max has to
-// move), per-lane partial row sums, and merges the warps at segment ends.
+// CTA = 12 warps.  One producer thread streams, for every unit, the 128 K rows
+// and 128 V rows of the block as 128-byte-swizzled TMA boxes (one per page and
+// 64-dim half) and, at the start of each (i, g), the G query rows, into a ring
+// of stages; it runs up to NS units ahead.  Eight consumer warps each take 16
+// of the block's keys.  The G query heads of the group are the rows of a
+// 16-row tile (GQA grouping: every K/V byte is read from HBM once per KV head),
+// and both contractions run on the warp-level tensor path (mma.sync m16n8k16,
+// f16 inputs, f32 accumulation): S = Q K^T for the warp's 16 keys, then
+// O += P V with P taken straight from the S registers.  The softmax is online
+// with quad shuffles and a lazy running max; warps merge at segment ends.  A
+// combining warp folds the splits of other CTAs.  Scalar FP32 FMAs plus f16 ->
+// f32 conversions could not keep up with HBM on this part (about 3200 issue
+// cycles of math per 128-key block against about 3000 cycles of HBM time),
+// which is why the two small contractions use the tensor path; tcgen05 and
+// TMEM stay with the prefill tiles.
 #include "kernels.cuh"
+#include "tc.cuh"
+#include "tmap.cuh"
 
 namespace pa {
 
-constexpr int kDecWarps = 16;                      // consumer warps (warpgroups 0-3)
-constexpr int kDecThreads = 20 * 32;               // warpgroup 4: producer, combiner, 2 idle
-constexpr int kDecRegsConsumer = 104;              // setmaxnreg split (per thread)
-constexpr int kDecRegsOther = 64;
+constexpr int kDecWarps = 8;                       // consumer warps (warpgroups 0, 1)
+constexpr int kDecThreads = 12 * 32;               // warpgroup 2: producer, combiner, 2 idle
+constexpr int kDecRegsConsumer = 216;              // setmaxnreg split (per thread)
+constexpr int kDecRegsOther = 72;
 // registers the split needs from the launch; checked on the host before launching
-constexpr int kDecRegsSplitTotal = 512 * kDecRegsConsumer + 128 * kDecRegsOther;
-constexpr int kKeysPerWarp = KB / kDecWarps;       // 8
+constexpr int kDecRegsSplitTotal = 256 * kDecRegsConsumer + 128 * kDecRegsOther;
+constexpr int kKeysPerWarp = KB / kDecWarps;       // 16
 constexpr float kDecRescale = 8.0f;                // lazy max: rescale when it grows by > 2^8
-static_assert(kKeysPerWarp == 8, "warp key slice is 8 rows");
+constexpr int kBox = KB * 128;                     // one 128-row x 64-dim swizzled box (16 KB)
+static_assert(kKeysPerWarp == 16, "warp key slice is 16 rows");
 
 template <int D, int G>
 struct DecCfg {
-  static constexpr int kBlk = KB * D * 2;                     // one block of K (or V)
-  static constexpr int kQ = ((G * D * 2) + 127) / 128 * 128;  // the group's query rows
-  static constexpr int kStage = 2 * kBlk + kQ;
-  static constexpr int kSbuf = kDecWarps * kKeysPerWarp * G * 4;
-  static constexpr int kMergeDims = 64;  // the warps merge 64 dims at a time
+  static constexpr int kHalves = D / 64;
+  static constexpr int kBlk = kHalves * kBox;                 // one block of K (or V)
+  static constexpr int kQ = ((G * D * 2) + 1023) / 1024 * 1024;  // the group's query rows
+  static constexpr int kStage = 2 * kBlk + kQ;                // multiple of 1024
+  static constexpr int kMergeDims = 64;                       // the warps merge 64 dims at a time
   static constexpr int kMerge = kDecWarps * G * (kMergeDims + 2) * 4;
-  static constexpr int kFixed = kSbuf + kMerge + 512;  // + barriers, jobs, flags, stage rows
-  static constexpr int kBudget = 227 * 1024 - 1024;
+  static constexpr int kFixed = kMerge + 512;                 // + barriers, jobs, flags
+  static constexpr int kBudget = 227 * 1024 - 2048;           // minus alignment slack
   static constexpr int NS0 = (kBudget - kFixed) / kStage;
   static constexpr int NS = NS0 > 6 ? 6 : NS0;
   static_assert(NS >= 2, "at least two stages");
-  static constexpr int kSmem = NS * kStage + kFixed;
+  static constexpr int kSmem = NS * kStage + kFixed + 1024;
 };
 
 constexpr int kJobs = 4;  // hand-off ring from the consumers to the combining warp
@@ -61,8 +69,9 @@ struct DecBars {
   uint64_t full[6], empty[6];
   uint64_t job_full[kJobs], job_empty[kJobs];
   DecJob jobs[kJobs];
-  int rows[6];   // valid keys of the block held by each stage
+  int rows[6];  // valid keys of the block held by each stage (0: skip the block)
   int abort;
+  int last;     // the consumers complete the split of the CTA's final segment
 };
 
 // Position in the unit sequence of this CTA.
@@ -92,11 +101,15 @@ __device__ __forceinline__ void it_token(UnitIt &it, int i, const DecView &v) {
   it.L = min(max(L, 0), v.cap);
 }
 
-// Iterator at the CTA's first unit, as placed by the planner: (i, g, kb).
-__device__ __forceinline__ void it_start(UnitIt &it, int4 st, const DecView &v) {
-  it_token(it, st.x, v);
-  it.g = st.y;
-  it.kb = st.z;
+// Iterator at the CTA's first unit, as placed by the planner: (i, g, kb, token) and
+// (units, kv_len) -- no dependent loads before the first copy.
+__device__ __forceinline__ void it_start(UnitIt &it, int4 s0, int4 s1) {
+  it.i = s0.x;
+  it.g = s0.y;
+  it.kb = s0.z;
+  it.tok = s0.w;
+  it.units = s1.x;
+  it.L = s1.y;
 }
 
 __device__ __forceinline__ void it_next(UnitIt &it, const DecView &v) {
@@ -129,72 +142,57 @@ __device__ __forceinline__ bool dec_wait(uint64_t *bar, uint32_t parity, int *er
   }
 }
 
-// Sum-reduce-scatter across the 8 lanes of a key group (xor 4, 2, 1).
-template <int N>
-__device__ __forceinline__ void rs_step(float *v, bool up, int m) {
-#pragma unroll
-  for (int j = 0; j < N / 2; ++j) {
-    float send = up ? v[j] : v[j + N / 2];
-    float keep = up ? v[j + N / 2] : v[j];
-    v[j] = keep + __shfl_xor_sync(0xffffffffu, send, m);
-  }
-}
-
-// Reductions over the lanes that hold the same heads (equal bit 0 of the lane).
-__device__ __forceinline__ float red_max_heads(float x) {
-  x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 2));
-  x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 4));
-  x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 8));
-  x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 16));
-  return x;
-}
-__device__ __forceinline__ float red_sum_heads(float x) {
-  x += __shfl_xor_sync(0xffffffffu, x, 2);
-  x += __shfl_xor_sync(0xffffffffu, x, 4);
-  x += __shfl_xor_sync(0xffffffffu, x, 8);
-  x += __shfl_xor_sync(0xffffffffu, x, 16);
-  return x;
-}
-
-// Barrier of the eight consumer warps only (the producer warp never joins).
+// Barrier of the consumer warps only (the producer warpgroup never joins).
 __device__ __forceinline__ void consumers_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kDecWarps * 32) : "memory");
 }
 
-// Sum (or max) of one value per head over all lanes of the warp: every lane
-// passes, for each head, its contribution (0 / -inf when it holds none).
-template <int G>
-__device__ __forceinline__ void warp_sum_heads(float (&x)[G]) {
-#pragma unroll
-  for (int h = 0; h < G; ++h)
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) x[h] += __shfl_xor_sync(0xffffffffu, x[h], m);
+// ---- warp-level tensor path helpers ---------------------------------------------
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                        uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
 }
-template <int G>
-__device__ __forceinline__ void warp_max_heads(float (&x)[G]) {
-#pragma unroll
-  for (int h = 0; h < G; ++h)
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) x[h] = fmaxf(x[h], __shfl_xor_sync(0xffffffffu, x[h], m));
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                          uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+// D = A(16x16, f16, row) * B(16x8, f16, col) + D, f32 accumulators
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// Byte offset of (row r, 16-byte chunk c) inside a 128-byte-swizzled box of 128-byte rows.
+__device__ __forceinline__ uint32_t sw128(int r, int c) {
+  return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
+}
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&h);
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(kDecThreads, 1) k_decode(AttnArgs a) {
+__global__ void __launch_bounds__(kDecThreads, 1)
+k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
   using Cfg = DecCfg<D, G>;
   constexpr int NS = Cfg::NS;
-  constexpr int LPK = D / 8;                // lanes per key row (one 16-byte chunk = 8 dims each)
-  constexpr int KPS = 32 / LPK;             // keys per step of the warp
-  constexpr int STEPS = kKeysPerWarp / KPS; // steps per unit
-  constexpr int DPL = D / 32;               // output dims per lane in the PV product
-  constexpr int NV = STEPS * G;             // partial scores per lane before the reduction
-  constexpr int NF = NV >= LPK ? NV / LPK : 1;  // scores per lane after the reduce-scatter
+  constexpr int KSTEPS = D / 16;  // k-steps of the QK contraction
+  constexpr int NT = D / 8;       // 8-dim tiles of the PV product
+  static_assert(G <= 8, "the group fits in rows 0..7 of the 16-row tile");
 
-  extern __shared__ __align__(128) unsigned char smem[];
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const uint32_t raw_s = smem_u32(smem_raw);
+  unsigned char *smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
   unsigned char *ring = smem;
-  float *sbuf_all = reinterpret_cast<float *>(smem + NS * Cfg::kStage);
-  float *merge = reinterpret_cast<float *>(smem + NS * Cfg::kStage + Cfg::kSbuf);
-  DecBars *bars =
-      reinterpret_cast<DecBars *>(smem + NS * Cfg::kStage + Cfg::kSbuf + Cfg::kMerge);
+  float *merge = reinterpret_cast<float *>(smem + NS * Cfg::kStage);
+  DecBars *bars = reinterpret_cast<DecBars *>(smem + NS * Cfg::kStage + Cfg::kMerge);
 
   WsHeader *hdr = reinterpret_cast<WsHeader *>(a.ws);
   int *err = &hdr->err;
@@ -219,7 +217,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(AttnArgs a) {
   const int u0 = (int)((int64_t)c * U / C), u1 = (int)((int64_t)(c + 1) * U / C);
   if (u0 >= u1) return;
   const int n = u1 - u0;
-  const int4 start = reinterpret_cast<const int4 *>(a.ws + a.lay.dec_start)[c];
+  const int4 start0 = reinterpret_cast<const int4 *>(a.ws + a.lay.dec_start)[2 * c];
+  const int4 start1 = reinterpret_cast<const int4 *>(a.ws + a.lay.dec_start)[2 * c + 1];
 
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   if (tid == 0) {
@@ -238,45 +237,68 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(AttnArgs a) {
   volatile int *abort = &bars->abort;
 
   if (w >= kDecWarps) {
-    // ------------------------------------------------------------------ producer
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kDecRegsOther));
     if (w == kDecWarps && lane == 0) {
+      // ---------------------------------------------------------------- producer
+      tc::prefetch_tmap(&maps.k);
+      tc::prefetch_tmap(&maps.v);
+      const int pages_per_block = KB / a.P;
+      const int oob_row = a.num_pages * a.Hkv * a.P;  // first row past the pool: zero fill
       UnitIt pit;
-      it_start(pit, start, v);
+      it_start(pit, start0, start1);
       int issued = 0;
+      // page ids of the unit about to be issued, loaded one unit ahead (while the
+      // producer waits for a free stage) so no global load sits on the issue path
+      int pgs[8];
+      int npg = 0;
+      auto fetch_pages = [&](const UnitIt &u) {
+        const int key0 = u.kb * KB;
+        const int rows = min(KB, u.L - key0);
+        npg = (rows + a.P - 1) / a.P;
+        const int32_t *row = a.tpt + (size_t)u.tok * a.max_pages + key0 / a.P;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) pgs[j] = j < npg ? row[j] : -1;
+      };
+      fetch_pages(pit);
       for (int k = 0; k < n; ++k) {
         const int st = k % NS;
         if (!dec_wait(&bars->empty[st], ((k / NS) & 1) ^ 1, err, abort)) break;
         unsigned char *stage = ring + st * Cfg::kStage;
-        const int key0 = pit.kb * KB;
-        int rows = min(KB, pit.L - key0);
-        // all pages of the block must exist, else the block is skipped (and flagged)
-        const int32_t *row = a.tpt + (size_t)pit.tok * a.max_pages + key0 / a.P;
-        const int npg = (rows + a.P - 1) / a.P;
-        for (int j = 0; j < npg; ++j) {
-          const int page = row[j];
-          if (page < 0 || page >= a.num_pages) {
+        int rows = min(KB, pit.L - pit.kb * KB);
+        // every page of the block must exist, else the block is skipped (and flagged)
+        int ys[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int page = pgs[j];
+          const bool bad = j < npg && (page < 0 || page >= a.num_pages);
+          if (bad) {
             atomicOr(err, PA_ERR_PAGE_RANGE);
             rows = 0;
-            break;
           }
+          ys[j] = (j < npg && !bad) ? (page * a.Hkv + pit.g) * a.P : oob_row;
         }
         const bool seg_first = (k == 0) || pit.kb == 0;
         bars->rows[st] = rows;
         const uint32_t qbytes = seg_first ? (uint32_t)(G * D * 2) : 0u;
-        mbar_arrive_expect_tx(&bars->full[st], 2u * rows * D * 2 + qbytes);
-        for (int j = 0; rows > 0 && j < npg; ++j) {
-          const int r = min(a.P, rows - j * a.P);
-          const int64_t src = ((int64_t)row[j] * a.Hkv + pit.g) * a.P * D;
-          bulk_g2s(stage + j * a.P * D * 2, a.k_pages + src, r * D * 2, &bars->full[st]);
-          bulk_g2s(stage + Cfg::kBlk + j * a.P * D * 2, a.v_pages + src, r * D * 2,
-                   &bars->full[st]);
+        mbar_arrive_expect_tx(&bars->full[st], 2u * Cfg::kBlk + qbytes);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (j >= pages_per_block) break;
+          // pages past the sequence (or a skipped block) load the zero-filled tail of the map
+          const int y = rows > 0 ? ys[j] : oob_row;
+          for (int hf = 0; hf < Cfg::kHalves; ++hf) {
+            tc::tma_load_2d(stage + hf * kBox + j * a.P * 128, &maps.k, hf * 64, y,
+                            &bars->full[st]);
+            tc::tma_load_2d(stage + Cfg::kBlk + hf * kBox + j * a.P * 128, &maps.v, hf * 64, y,
+                            &bars->full[st]);
+          }
         }
         if (seg_first)
           bulk_g2s(stage + 2 * Cfg::kBlk, a.q + ((size_t)pit.tok * a.Hq + pit.g * G) * D, qbytes,
                    &bars->full[st]);
         ++issued;
         it_next(pit, v);
+        if (k + 1 < n) fetch_pages(pit);
       }
       // after giving up, let copies already in flight land before the CTA exits
       if (*abort) {
@@ -361,40 +383,26 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(AttnArgs a) {
 
   // -------------------------------------------------------------------- consumers
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kDecRegsConsumer));
-  const int rl = lane % LPK, kq = lane / LPK;
-  float *sbuf = sbuf_all + w * kKeysPerWarp * G;
-  // After the reduce-scatter over the LPK lanes of a key, this lane holds NF
-  // consecutive score indices starting at vbase (index = step * G + head); lanes
-  // that differ only in bits of `dup` hold duplicates (levels where fewer values
-  // than lanes were left are all-reduced instead of scattered).
-  int vbase = 0, dup = 0;
-  {
-    int cnt = NV;
-#pragma unroll
-    for (int m = LPK / 2; m >= 1; m >>= 1) {
-      if (cnt >= 2) {
-        if (rl & m) vbase += cnt / 2;
-        cnt /= 2;
-      } else {
-        dup |= m;
-      }
-    }
-  }
-  const bool primary = (rl & dup) == 0;
+  // fragment coordinates: this lane holds rows (heads) r = lane/4 and r + 8 (padding),
+  // and columns 2*(lane%4) + {0, 1} of each 8-column tile
+  const int hr = lane >> 2, cq = lane & 3;
+  const bool head_lane = hr < G;
+  const int key_base = w * kKeysPerWarp;
 
   UnitIt cit;
-  it_start(cit, start, v);
+  it_start(cit, start0, start1);
   int seg_begin = 0;
-  float qf[G][8];
-  float m_run[G];    // running max per head (log2 domain), replicated in all lanes
-  float l_part[G];   // this lane's partial row sums per head (primary lanes only)
-  float acc[G][DPL];
+  uint32_t qa[KSTEPS][2];  // A fragments of Q: columns 2cq.. and 8+2cq.. of each k-step
+  float o[NT][4];          // O accumulators (rows hr and hr + 8)
+  float m_run = -INFINITY; // running max of head hr (log2 domain)
+  float l_part = 0.f;      // this lane's share of the row sum of head hr
   bool dead = false;
-  int n_jobs = 0;  // partials handed to the combining warp
+  int n_jobs = 0;          // partials handed to the combining warp
 
   for (int k = 0; k < n; ++k) {
     const int st = k % NS;
     unsigned char *stage = ring + st * Cfg::kStage;
+    const uint32_t sK = smem_u32(stage), sV = smem_u32(stage + Cfg::kBlk);
     const bool seg_first = (k == 0) || cit.kb == 0;
     const bool seg_last = (k == n - 1) || cit.kb + 1 == cit.units;
     if (!dead) dead = !dec_wait(&bars->full[st], (k / NS) & 1, err, abort);
@@ -404,157 +412,91 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(AttnArgs a) {
       seg_begin = a.Hkv * v.tok_unit_off[cit.i] + cit.g * cit.units;
       const uint16_t *qs = reinterpret_cast<const uint16_t *>(stage + 2 * Cfg::kBlk);
 #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        uint4 q4 = dead ? make_uint4(0, 0, 0, 0)
-                        : *reinterpret_cast<const uint4 *>(qs + h * D + rl * 8);
-        float2 f0 = h2_to_f2(q4.x), f1 = h2_to_f2(q4.y), f2 = h2_to_f2(q4.z), f3 = h2_to_f2(q4.w);
-        qf[h][0] = f0.x * a.scale_log2; qf[h][1] = f0.y * a.scale_log2;
-        qf[h][2] = f1.x * a.scale_log2; qf[h][3] = f1.y * a.scale_log2;
-        qf[h][4] = f2.x * a.scale_log2; qf[h][5] = f2.y * a.scale_log2;
-        qf[h][6] = f3.x * a.scale_log2; qf[h][7] = f3.y * a.scale_log2;
-        m_run[h] = -INFINITY;
-        l_part[h] = 0.f;
-#pragma unroll
-        for (int e = 0; e < DPL; ++e) acc[h][e] = 0.f;
+      for (int ks = 0; ks < KSTEPS; ++ks) {
+        qa[ks][0] = (head_lane && !dead)
+                        ? *reinterpret_cast<const uint32_t *>(qs + hr * D + ks * 16 + 2 * cq)
+                        : 0u;
+        qa[ks][1] = (head_lane && !dead)
+                        ? *reinterpret_cast<const uint32_t *>(qs + hr * D + ks * 16 + 8 + 2 * cq)
+                        : 0u;
       }
+#pragma unroll
+      for (int t = 0; t < NT; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
+      m_run = -INFINITY;
+      l_part = 0.f;
     }
 
-    const int nr = min(max(rows - w * kKeysPerWarp, 0), kKeysPerWarp);
+    const int nr = min(max(rows - key_base, 0), kKeysPerWarp);
+    bool zeroed = false;
     if (nr > 0) {
-      const uint16_t *Ks = reinterpret_cast<const uint16_t *>(stage) + w * kKeysPerWarp * D;
-      const uint16_t *Vs =
-          reinterpret_cast<const uint16_t *>(stage + Cfg::kBlk) + w * kKeysPerWarp * D;
-      // ---- scores: STEPS steps of KPS keys; LPK lanes per key, one 16-byte chunk each
-      float vals[NV];
+      // ---- S = Q K^T for the warp's 16 keys (two 8-key tiles), f32 accumulators
+      float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      // ldmatrix x4 row addresses: matrix = lane / 8 -> (key half, dim half)
+      const int lm_key = key_base + ((lane >> 4) << 3) + (lane & 7);
+      const int lm_chunk = (lane >> 3) & 1;
 #pragma unroll
-      for (int s = 0; s < STEPS; ++s) {
-        const int r = s * KPS + kq;
-        uint4 k4 = *reinterpret_cast<const uint4 *>(Ks + r * D + rl * 8);
-        float2 k0 = h2_to_f2(k4.x), k1 = h2_to_f2(k4.y), k2 = h2_to_f2(k4.z), k3 = h2_to_f2(k4.w);
+      for (int ks = 0; ks < KSTEPS; ++ks) {
+        const int box = ks >> 2, chunk = (ks & 3) * 2 + lm_chunk;
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(sK + box * kBox + sw128(lm_key, chunk), b0, b1, b2, b3);
+        mma16816(s[0], qa[ks][0], 0u, qa[ks][1], 0u, b0, b1);
+        mma16816(s[1], qa[ks][0], 0u, qa[ks][1], 0u, b2, b3);
+      }
+      // ---- online softmax on the fragment: this lane has keys 2cq, 2cq+1 (+8) of head hr
+      float x[4];
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          float2 p2 = make_float2(qf[h][0] * k0.x, qf[h][1] * k0.y);
-          p2 = ffma2(make_float2(qf[h][2], qf[h][3]), k1, p2);
-          p2 = ffma2(make_float2(qf[h][4], qf[h][5]), k2, p2);
-          p2 = ffma2(make_float2(qf[h][6], qf[h][7]), k3, p2);
-          vals[s * G + h] = p2.x + p2.y;
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int kk = t * 8 + 2 * cq + e;
+          x[t * 2 + e] = (kk < nr) ? s[t][e] * a.scale_log2 : -INFINITY;
+        }
+      const float xm = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+      if (__any_sync(0xffffffffu, xm > m_run + kDecRescale)) {
+        // the running max moves: exact block max of the row (its quad), rescale
+        float bm = fmaxf(xm, __shfl_xor_sync(0xffffffffu, xm, 1));
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
+        const float m_new = fmaxf(m_run, bm);
+        const float alpha = (m_run == -INFINITY) ? 0.f : exp2_approx(m_run - m_new);
+        m_run = m_new;
+        l_part *= alpha;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          o[t][0] *= alpha;
+          o[t][1] *= alpha;
         }
       }
-      // ---- sum over the LPK lanes of each key: scatter while values last, then all-reduce
-      {
-        int cnt = NV;
+      const float m_use = m_run == -INFINITY ? 0.f : m_run;
+      float p[4];
 #pragma unroll
-        for (int m = LPK / 2; m >= 1; m >>= 1) {
-          if (cnt >= 2) {
-            const bool up = (rl & m) != 0;
-#pragma unroll
-            for (int j = 0; j < NV / 2; ++j) {
-              if (j < cnt / 2) {
-                const float send = up ? vals[j] : vals[j + cnt / 2];
-                const float keep = up ? vals[j + cnt / 2] : vals[j];
-                vals[j] = keep + __shfl_xor_sync(0xffffffffu, send, m);
-              }
-            }
-            cnt /= 2;
-          } else {
-            vals[0] += __shfl_xor_sync(0xffffffffu, vals[0], m);
-          }
-        }
+      for (int j = 0; j < 4; ++j) p[j] = exp2_approx(x[j] - m_use);  // -inf -> 0
+      l_part += (p[0] + p[1]) + (p[2] + p[3]);
+      // P as the A fragment of the PV product (k = the warp's 16 keys; rows 8..15 zero)
+      const uint32_t pa0 = pack_h2(p[0], p[1]), pa2 = pack_h2(p[2], p[3]);
+      // V rows past the valid keys may hold stale data or NaN: zero them (0 * NaN)
+      if (nr < kKeysPerWarp) {
+        for (int r = key_base + nr + (lane >> 3); r < key_base + kKeysPerWarp; r += 4)
+          for (int hf = 0; hf < Cfg::kHalves; ++hf)
+            reinterpret_cast<uint4 *>(stage + Cfg::kBlk + hf * kBox + r * 128)[lane & 7] =
+                make_uint4(0, 0, 0, 0);
+        __syncwarp();
+        zeroed = true;
       }
-      // ---- masking (select, so stale or NaN rows never count) and the lazy max
-      float x[NF];
-      int hj[NF], kj[NF];
-      bool need = false;
+      // ---- O += P V, 8 dims per tile; ldmatrix.trans gives the V fragments
+      const int lt_key = key_base + (((lane >> 3) & 1) << 3) + (lane & 7);
+      const int lt_tile = lane >> 4;
 #pragma unroll
-      for (int j = 0; j < NF; ++j) {
-        const int vi = vbase + j;
-        const int s = vi / G;
-        hj[j] = vi - s * G;
-        kj[j] = s * KPS + kq;
-        x[j] = kj[j] < nr ? vals[j] : -INFINITY;
-        float mr = 0.f;
-#pragma unroll
-        for (int h = 0; h < G; ++h)
-          if (h == hj[j]) mr = m_run[h];
-        need |= x[j] > mr + kDecRescale;  // also true while m_run is -inf
-      }
-      if (__any_sync(0xffffffffu, need)) {
-        // the running max moves: exact block max per head, rescale what was summed
-        float bm[G];
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          bm[h] = -INFINITY;
-#pragma unroll
-          for (int j = 0; j < NF; ++j)
-            if (hj[j] == h) bm[h] = fmaxf(bm[h], x[j]);
-        }
-        warp_max_heads<G>(bm);
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float m_new = fmaxf(m_run[h], bm[h]);
-          const float alpha = (m_run[h] == -INFINITY) ? 0.f : exp2_approx(m_run[h] - m_new);
-          m_run[h] = m_new;
-          l_part[h] *= alpha;
-#pragma unroll
-          for (int e = 0; e < DPL; ++e) acc[h][e] *= alpha;
-        }
-      }
-      // ---- p = 2^(x - m) into the per-warp buffer; partial sums stay in the lane
-#pragma unroll
-      for (int j = 0; j < NF; ++j) {
-        float mr = 0.f;
-#pragma unroll
-        for (int h = 0; h < G; ++h)
-          if (h == hj[j]) mr = m_run[h];
-        const float p = (x[j] == -INFINITY) ? 0.f : exp2_approx(x[j] - mr);
-        if (primary) {
-#pragma unroll
-          for (int h = 0; h < G; ++h)
-            if (h == hj[j]) l_part[h] += p;
-          sbuf[kj[j] * G + hj[j]] = p;
-        }
-      }
-      __syncwarp();
-      // ---- PV: lane owns dims [DPL*lane, DPL*lane + DPL) of every head
-#pragma unroll
-      for (int jj = 0; jj < kKeysPerWarp; ++jj) {
-        if (jj < nr) {
-          float pr[G];
-          if constexpr (G % 4 == 0) {
-#pragma unroll
-            for (int h = 0; h < G; h += 4) {
-              float4 t4 = *reinterpret_cast<const float4 *>(sbuf + jj * G + h);
-              pr[h] = t4.x; pr[h + 1] = t4.y; pr[h + 2] = t4.z; pr[h + 3] = t4.w;
-            }
-          } else if constexpr (G == 2) {
-            float2 t2 = *reinterpret_cast<const float2 *>(sbuf + jj * 2);
-            pr[0] = t2.x; pr[1] = t2.y;
-          } else {
-            pr[0] = sbuf[jj];
-          }
-          if constexpr (DPL == 4) {
-            uint2 v2 = *reinterpret_cast<const uint2 *>(Vs + jj * D + 4 * lane);
-            float2 v01 = h2_to_f2(v2.x), v23 = h2_to_f2(v2.y);
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-              float2 a01 = ffma2(make_float2(pr[h], pr[h]), v01, make_float2(acc[h][0], acc[h][1]));
-              float2 a23 = ffma2(make_float2(pr[h], pr[h]), v23, make_float2(acc[h][2], acc[h][3]));
-              acc[h][0] = a01.x; acc[h][1] = a01.y; acc[h][2] = a23.x; acc[h][3] = a23.y;
-            }
-          } else {
-            uint32_t v1 = *reinterpret_cast<const uint32_t *>(Vs + jj * D + 2 * lane);
-            float2 v01 = h2_to_f2(v1);
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-              float2 a01 = ffma2(make_float2(pr[h], pr[h]), v01, make_float2(acc[h][0], acc[h][1]));
-              acc[h][0] = a01.x; acc[h][1] = a01.y;
-            }
-          }
-        }
+      for (int t = 0; t < NT; t += 2) {
+        const int dchunk = t + lt_tile;  // 16-byte chunk = 8-dim tile
+        const int box = dchunk >> 3, chunk = dchunk & 7;
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(sV + box * kBox + sw128(lt_key, chunk), b0, b1, b2, b3);
+        mma16816(o[t], pa0, 0u, pa2, 0u, b0, b1);
+        mma16816(o[t + 1], pa0, 0u, pa2, 0u, b2, b3);
       }
     }
+    if (zeroed) fence_proxy_async();  // generic writes before async copies refill the stage
     __syncwarp();
-
     // the stage's K/V are consumed: release it now, so the producer keeps streaming
     // while the warps merge below
     if (lane == 0) mbar_arrive(&bars->empty[st]);
@@ -566,16 +508,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(AttnArgs a) {
       float *mw = merge;                  // [warps][G]
       float *lw = mw + kDecWarps * G;     // [warps][G]
       float *aw = lw + kDecWarps * G;     // [warps][G][MD]
-      float ls[G];
-#pragma unroll
-      for (int h = 0; h < G; ++h) ls[h] = l_part[h];
-      warp_sum_heads<G>(ls);
-      if (lane == 0) {
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          mw[w * G + h] = m_run[h];
-          lw[w * G + h] = ls[h];
-        }
+      float ls = l_part;
+      ls += __shfl_xor_sync(0xffffffffu, ls, 1);
+      ls += __shfl_xor_sync(0xffffffffu, ls, 2);
+      if (head_lane && cq == 0) {
+        mw[w * G + hr] = m_run;
+        lw[w * G + hr] = ls;
       }
       const int seg_units = cit.units;
       const bool direct = seg_begin >= u0 && seg_begin + seg_units <= u1;
@@ -583,12 +521,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(AttnArgs a) {
       const int slot = ig + c;
 #pragma unroll
       for (int d0 = 0; d0 < D; d0 += MD) {
-        // lane owns dims [DPL*lane, DPL*lane + DPL): those inside [d0, d0 + MD) go in
-        if (DPL * lane >= d0 && DPL * lane < d0 + MD) {
+        if (head_lane) {
 #pragma unroll
-          for (int h = 0; h < G; ++h)
-#pragma unroll
-            for (int e = 0; e < DPL; ++e) aw[(w * G + h) * MD + DPL * lane - d0 + e] = acc[h][e];
+          for (int t = d0 / 8; t < (d0 + MD) / 8; ++t) {
+            aw[(w * G + hr) * MD + t * 8 - d0 + 2 * cq] = o[t][0];
+            aw[(w * G + hr) * MD + t * 8 - d0 + 2 * cq + 1] = o[t][1];
+          }
         }
         consumers_sync();
         for (int idx = tid; idx < G * MD; idx += kDecWarps * 32) {
@@ -596,29 +534,77 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(AttnArgs a) {
           float M = -INFINITY;
 #pragma unroll
           for (int xw = 0; xw < kDecWarps; ++xw) M = fmaxf(M, mw[xw * G + h]);
-          float o = 0.f, Ls = 0.f;
+          float oo = 0.f, Ls = 0.f;
           if (M != -INFINITY) {
 #pragma unroll
             for (int xw = 0; xw < kDecWarps; ++xw) {
               const float mx = mw[xw * G + h];
               const float f = mx == -INFINITY ? 0.f : exp2_approx(mx - M);
-              o += f * aw[(xw * G + h) * MD + dd - d0];
+              oo += f * aw[(xw * G + h) * MD + dd - d0];
               Ls += f * lw[xw * G + h];
             }
           }
           if (direct) {
-            const float r = Ls > 0.f ? o / Ls : 0.f;
+            const float r = Ls > 0.f ? oo / Ls : 0.f;
             a.out[((size_t)cit.tok * a.Hq + cit.g * G + h) * D + dd] =
                 __half_as_ushort(__float2half_rn(r));
           } else {
             float *pp = partials + ((size_t)slot * G + h) * (D + 2);
-            pp[2 + dd] = o;
+            pp[2 + dd] = oo;
             if (dd == 0) { pp[0] = M; pp[1] = Ls; }
           }
         }
         consumers_sync();  // the merge area may be rewritten
       }
-      if (!direct && tid == 0) {
+      if (!direct && k == n - 1) {
+        // The CTA's final segment continues into the next CTA, which handled its part
+        // first, so this CTA is almost always the last to arrive; everyone else is
+        // done too, so the consumers fold the parts right here, all loads at once.
+        const int64_t ub = seg_begin, ue = ub + seg_units;
+        const int c_first = cta_of_unit(ub, U, C), c_last = cta_of_unit(ue - 1, U, C);
+        int n_parts = 0;
+        for (int cc = c_first; cc <= c_last; ++cc) n_parts += cta_has_units(cc, U, C) ? 1 : 0;
+        if (tid == 0) {
+          __threadfence();  // the partial of every consumer is visible before the count
+          bars->last = atomicAdd(&dec_cnt[ig], 1) == n_parts - 1;
+        }
+        consumers_sync();
+        if (bars->last) {
+          __threadfence();
+          for (int idx = tid; idx < G * D; idx += kDecWarps * 32) {
+            const int h = idx / D, dd = idx - h * D;
+            float M = -INFINITY, Ls = 0.f, oo = 0.f;
+            for (int c0 = c_first; c0 <= c_last; c0 += 8) {
+              float mp[8], lp[8], op[8];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {  // issue every load of the batch first
+                const int cc = c0 + j;
+                const bool use = cc <= c_last && cta_has_units(cc, U, C);
+                const float *pp = partials + ((size_t)(ig + (use ? cc : c_first)) * G + h) * (D + 2);
+                mp[j] = use ? __ldcg(pp) : -INFINITY;
+                lp[j] = use ? __ldcg(pp + 1) : 0.f;
+                op[j] = use ? __ldcg(pp + 2 + dd) : 0.f;
+              }
+              float Mn = M;
+#pragma unroll
+              for (int j = 0; j < 8; ++j) Mn = fmaxf(Mn, mp[j]);
+              const float fo = M == -INFINITY ? 0.f : exp2_approx(M - Mn);
+              Ls *= fo;
+              oo *= fo;
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const float f = mp[j] == -INFINITY ? 0.f : exp2_approx(mp[j] - Mn);
+                Ls += f * lp[j];
+                oo += f * op[j];
+              }
+              M = Mn;
+            }
+            a.out[((size_t)cit.tok * a.Hq + cit.g * G + h) * D + dd] =
+                __half_as_ushort(__float2half_rn(Ls > 0.f ? oo / Ls : 0.f));
+          }
+          if (tid == 0) dec_cnt[ig] = 0;  // ready for the next run of this plan
+        }
+      } else if (!direct && tid == 0) {
         // hand the cross-CTA combine to the combining warp
         const int q = n_jobs % kJobs;
         if (dec_wait(&bars->job_empty[q], ((n_jobs / kJobs) & 1) ^ 1, err, abort)) {
@@ -633,7 +619,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(AttnArgs a) {
           mbar_arrive(&bars->job_full[q]);
         }
       }
-      if (!direct) ++n_jobs;
+      if (!direct && k != n - 1) ++n_jobs;
     }
     it_next(cit, v);
   }
@@ -647,7 +633,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(AttnArgs a) {
 }
 
 template <int D, int G>
-static cudaError_t launch_decode_t(const AttnArgs &a, int num_sms, cudaStream_t s) {
+static cudaError_t launch_decode_t(const AttnArgs &a, int num_sms, const AttnMaps *maps,
+                                   cudaStream_t s) {
   using Cfg = DecCfg<D, G>;
   static bool attr_set = false;
   if (!attr_set) {
@@ -662,14 +649,15 @@ static cudaError_t launch_decode_t(const AttnArgs &a, int num_sms, cudaStream_t 
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  k_decode<D, G><<<num_sms, kDecThreads, Cfg::kSmem, s>>>(a);
+  k_decode<D, G><<<num_sms, kDecThreads, Cfg::kSmem, s>>>(a, *maps);
   return cudaGetLastError();
 }
 
-cudaError_t launch_decode(const AttnArgs &a, int num_sms, cudaStream_t s) {
+cudaError_t launch_decode(const AttnArgs &a, int num_sms, const void *tmaps, cudaStream_t s) {
+  const AttnMaps *maps = static_cast<const AttnMaps *>(tmaps);
   const int G = a.Hq / a.Hkv;
 #define PA_DEC_CASE(DD, GG) \
-  if (a.D == DD && G == GG) return launch_decode_t<DD, GG>(a, num_sms, s);
+  if (a.D == DD && G == GG) return launch_decode_t<DD, GG>(a, num_sms, maps, s);
   PA_DEC_CASE(128, 1) PA_DEC_CASE(128, 2) PA_DEC_CASE(128, 4) PA_DEC_CASE(128, 8)
   PA_DEC_CASE(64, 1) PA_DEC_CASE(64, 2) PA_DEC_CASE(64, 4) PA_DEC_CASE(64, 8)
 #undef PA_DEC_CASE

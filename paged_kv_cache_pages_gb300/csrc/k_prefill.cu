@@ -145,7 +145,7 @@ __device__ __forceinline__ bool seg_next(Seg &s, const SegCtx &x) {
 
 template <int D>
 __global__ void __launch_bounds__(kPfThreads, 1)
-k_prefill(AttnArgs a, const __grid_constant__ PrefillMaps maps) {
+k_prefill(AttnArgs a, const __grid_constant__ AttnMaps maps) {
   using Cfg = PfCfg<D>;
   // row record of a split part: O[D] | m | l | pad -- a multiple of 16 bytes so that
   // every row's record starts 16-byte aligned for float4 access
@@ -636,7 +636,7 @@ k_prefill(AttnArgs a, const __grid_constant__ PrefillMaps maps) {
 }
 
 template <int D>
-static cudaError_t launch_prefill_t(const AttnArgs &a, int num_sms, const PrefillMaps *maps,
+static cudaError_t launch_prefill_t(const AttnArgs &a, int num_sms, const AttnMaps *maps,
                                     cudaStream_t s) {
   using Cfg = PfCfg<D>;
   static bool attr_set = false;
@@ -656,7 +656,7 @@ static cudaError_t launch_prefill_t(const AttnArgs &a, int num_sms, const Prefil
 }
 
 cudaError_t launch_prefill(const AttnArgs &a, int num_sms, const void *tmaps, cudaStream_t s) {
-  const PrefillMaps *maps = static_cast<const PrefillMaps *>(tmaps);
+  const AttnMaps *maps = static_cast<const AttnMaps *>(tmaps);
   if (a.D == 128) return launch_prefill_t<128>(a, num_sms, maps, s);
   if (a.D == 64) return launch_prefill_t<64>(a, num_sms, maps, s);
   return cudaErrorInvalidValue;

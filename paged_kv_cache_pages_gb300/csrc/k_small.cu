@@ -285,7 +285,10 @@ k_plan(const int32_t *__restrict__ tpt, int max_pages, const int32_t *__restrict
       }
       long long r = u - (long long)Hkv * tok_unit_off[i];
       int g = units > 0 ? (int)(r / units) : 0;
-      dec_start[c] = make_int4(i, g, units > 0 ? (int)(r - (long long)g * units) : 0, 0);
+      const int tok = dec_tok[i];
+      const int L = min(max(kv[tok], 0), cap);
+      dec_start[2 * c] = make_int4(i, g, units > 0 ? (int)(r - (long long)g * units) : 0, tok);
+      dec_start[2 * c + 1] = make_int4(units, L, 0, 0);
     }
     if (W > 0) {
       long long w = (long long)c * W / C;

@@ -33,7 +33,7 @@ struct AttnArgs {
 
 // Decode: split-KV over all SMs plus the log-sum-exp reduce.  Returns a
 // cudaError_t from the launches.
-cudaError_t launch_decode(const AttnArgs &a, int num_sms, cudaStream_t s);
+cudaError_t launch_decode(const AttnArgs &a, int num_sms, const void *tmaps, cudaStream_t s);
 
 // Prefill: tcgen05 tensor-core tiles.
 cudaError_t launch_prefill(const AttnArgs &a, int num_sms, const void *tmaps, cudaStream_t s);

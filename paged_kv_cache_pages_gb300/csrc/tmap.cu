@@ -24,7 +24,7 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 
 }  // namespace
 
-int encode_prefill_maps(const AttnArgs &a, PrefillMaps *m) {
+int encode_attn_maps(const AttnArgs &a, AttnMaps *m) {
   auto enc = get_encode();
   if (!enc) return PA_ELAUNCH;
   const cuuint32_t estr[3] = {1, 1, 1};

@@ -1,4 +1,4 @@
-// TMA tensor maps of the prefill kernel (host-side encoding through the
+// TMA tensor maps of the attention kernels (host-side encoding through the
 // driver entry point, so the library needs no link-time libcuda).
 #pragma once
 
@@ -8,12 +8,12 @@
 
 namespace pa {
 
-struct PrefillMaps {
+struct AttnMaps {
   CUtensorMap q;  // 3-D {d, Hq, T}, box {64, 1, 128}, 128-byte swizzle
   CUtensorMap k;  // 2-D {d, num_pages * Hkv * P}, box {64, P}, 128-byte swizzle
   CUtensorMap v;
 };
 
-int encode_prefill_maps(const AttnArgs &a, PrefillMaps *m);
+int encode_attn_maps(const AttnArgs &a, AttnMaps *m);
 
 }  // namespace pa
