@@ -236,9 +236,15 @@ class DecodeBench:
 
 # ----------------------------------------------------------------------------- timing
 
+SPIN_CYCLES = 4_000_000   # about 2 ms at the maximum SM clock
+
+
 def time_steps(torch, fn, steps, warmup, world, per_launch=None):
     """Warm up, then time exactly `steps` calls of fn between barrier+sync pairs.
-    per_launch: number of (start, end) event pairs to record per step (kernel timing)."""
+    per_launch: number of (start, end) event pairs to record per step (kernel timing).
+    In that mode each step is queued behind a short device-side spin, so the host has
+    queued the whole step before the GPU reaches it and the event pairs time the
+    kernels, not the host's launch rate."""
     for _ in range(warmup):
         fn(None) if per_launch else fn()
     torch.cuda.synchronize()
@@ -253,6 +259,7 @@ def time_steps(torch, fn, steps, warmup, world, per_launch=None):
             pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                      for _ in range(per_launch)]
             ev_pairs.append(pairs)
+            torch.cuda._sleep(SPIN_CYCLES)
             fn(pairs)
         else:
             fn()
@@ -392,7 +399,8 @@ def run_ours(args):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": pb.launches_per_step * args.steps,
         "timing": "value: CUDA-graph replay of whole steps; roofline: per-launch CUDA events "
-                  "in a non-graph pass of the same steps",
+                  "in a non-graph pass of the same steps, each step queued behind a "
+                  "device-side spin so that host launch rate does not enter",
         "clocks": clocks,
         "decode": {"workload": "decode_8seq", "value": round(d_value, 1), "unit": "GB/s",
                    "layers": db.layers, "kv_bytes_per_layer": db.bytes_per_layer,

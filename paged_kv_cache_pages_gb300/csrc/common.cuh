@@ -20,7 +20,8 @@ namespace pa {
 //   flags          int  [T]      plan scratch: run-start flags
 //   runs           int  [T + 1]  plan scratch: first token of each run
 //   tile_off       int  [T + 1]  prefix sums of prefill work (key blocks x items) per tile
-//   dec_start      int4 [2C]     first decode unit of each CTA: (i, g, kb, token), (units, kv_len, -, -)
+//   dec_start      int4 [4C]     first decode unit of each CTA: (i, g, kb, token), (units, kv_len, -, -),
+//                                  then the page ids of that unit's key block (8 ints, -1 past its end)
 //   pf_start       int4 [C]      first prefill unit of each CTA: (tile, item in tile, kb, -)
 //   pf_cnt         int  [T * Hkv * NP * 2 * 4]  arrival counters of split prefill items,
 //                                  one per (item, softmax warpgroup, warp)
@@ -66,7 +67,7 @@ __host__ __device__ inline WsLayout ws_layout(int T, int Hq, int Hkv, int D, int
   l.flags = o;        o = align_up(o + Tm * 4, 256);
   l.runs = o;         o = align_up(o + (Tm + 1) * 4, 256);
   l.tile_off = o;     o = align_up(o + (Tm + 1) * 4, 256);
-  l.dec_start = o;    o = align_up(o + (size_t)C * 32, 256);
+  l.dec_start = o;    o = align_up(o + (size_t)C * 64, 256);
   l.pf_start = o;     o = align_up(o + (size_t)C * 16, 256);
   l.n_cnt = (int)(Tm * Hkv * NP * 8);
   l.pf_cnt = o;       o = align_up(o + (size_t)l.n_cnt * 4, 256);

@@ -194,6 +194,27 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
   float *merge = reinterpret_cast<float *>(smem + NS * Cfg::kStage);
   DecBars *bars = reinterpret_cast<DecBars *>(smem + NS * Cfg::kStage + Cfg::kMerge);
 
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], kDecWarps);
+    }
+    for (int j = 0; j < kJobs; ++j) {
+      mbar_init(&bars->job_full[j], 1);
+      mbar_init(&bars->job_empty[j], 1);
+    }
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (w == kDecWarps && lane == 0) {
+    tc::prefetch_tmap(&maps.k);
+    tc::prefetch_tmap(&maps.v);
+  }
+  // Launched as a programmatic dependent of the append kernel: the launch and the
+  // setup above overlap its tail; nothing written by earlier kernels is read before here.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  __syncthreads();
   WsHeader *hdr = reinterpret_cast<WsHeader *>(a.ws);
   int *err = &hdr->err;
   DecView v;
@@ -217,31 +238,15 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
   const int u0 = (int)((int64_t)c * U / C), u1 = (int)((int64_t)(c + 1) * U / C);
   if (u0 >= u1) return;
   const int n = u1 - u0;
-  const int4 start0 = reinterpret_cast<const int4 *>(a.ws + a.lay.dec_start)[2 * c];
-  const int4 start1 = reinterpret_cast<const int4 *>(a.ws + a.lay.dec_start)[2 * c + 1];
+  const int4 *start = reinterpret_cast<const int4 *>(a.ws + a.lay.dec_start) + 4 * c;
+  const int4 start0 = start[0], start1 = start[1];
 
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  if (tid == 0) {
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(&bars->full[s], 1);
-      mbar_init(&bars->empty[s], kDecWarps);
-    }
-    for (int j = 0; j < kJobs; ++j) {
-      mbar_init(&bars->job_full[j], 1);
-      mbar_init(&bars->job_empty[j], 1);
-    }
-    bars->abort = 0;
-    fence_mbar_init();
-  }
-  __syncthreads();
   volatile int *abort = &bars->abort;
 
   if (w >= kDecWarps) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kDecRegsOther));
     if (w == kDecWarps && lane == 0) {
       // ---------------------------------------------------------------- producer
-      tc::prefetch_tmap(&maps.k);
-      tc::prefetch_tmap(&maps.v);
       const int pages_per_block = KB / a.P;
       const int oob_row = a.num_pages * a.Hkv * a.P;  // first row past the pool: zero fill
       UnitIt pit;
@@ -259,7 +264,12 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) pgs[j] = j < npg ? row[j] : -1;
       };
-      fetch_pages(pit);
+      {  // the first unit's page ids come with its start record
+        const int4 p0 = start[2], p1 = start[3];
+        npg = (min(KB, pit.L - pit.kb * KB) + a.P - 1) / a.P;
+        pgs[0] = p0.x; pgs[1] = p0.y; pgs[2] = p0.z; pgs[3] = p0.w;
+        pgs[4] = p1.x; pgs[5] = p1.y; pgs[6] = p1.z; pgs[7] = p1.w;
+      }
       for (int k = 0; k < n; ++k) {
         const int st = k % NS;
         if (!dec_wait(&bars->empty[st], ((k / NS) & 1) ^ 1, err, abort)) break;
@@ -649,8 +659,17 @@ static cudaError_t launch_decode_t(const AttnArgs &a, int num_sms, const AttnMap
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  k_decode<D, G><<<num_sms, kDecThreads, Cfg::kSmem, s>>>(a, *maps);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_sms);
+  cfg.blockDim = dim3(kDecThreads);
+  cfg.dynamicSmemBytes = Cfg::kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_decode<D, G>, a, *maps);
 }
 
 cudaError_t launch_decode(const AttnArgs &a, int num_sms, const void *tmaps, cudaStream_t s) {

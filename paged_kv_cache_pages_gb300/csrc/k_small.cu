@@ -49,6 +49,9 @@ __global__ void k_append(const uint4 *__restrict__ k, const uint4 *__restrict__ 
                          const int64_t *__restrict__ slot, int T, uint4 *__restrict__ kp,
                          uint4 *__restrict__ vp, int num_pages, int Hkv, int P, int chunks_per_row,
                          int *err) {
+  // a following attention kernel may be launched now; it waits for this grid's
+  // results (griddepcontrol.wait) before it reads the pool
+  asm volatile("griddepcontrol.launch_dependents;");
   int64_t total = (int64_t)T * Hkv * chunks_per_row;
   int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
@@ -287,8 +290,16 @@ k_plan(const int32_t *__restrict__ tpt, int max_pages, const int32_t *__restrict
       int g = units > 0 ? (int)(r / units) : 0;
       const int tok = dec_tok[i];
       const int L = min(max(kv[tok], 0), cap);
-      dec_start[2 * c] = make_int4(i, g, units > 0 ? (int)(r - (long long)g * units) : 0, tok);
-      dec_start[2 * c + 1] = make_int4(units, L, 0, 0);
+      const int kb = units > 0 ? (int)(r - (long long)g * units) : 0;
+      dec_start[4 * c] = make_int4(i, g, kb, tok);
+      dec_start[4 * c + 1] = make_int4(units, L, 0, 0);
+      // page ids of the first key block, so the first copy needs no table lookup
+      int pg[8];
+      const int key0 = kb * KB, npg = (min(KB, L - key0) + P - 1) / P;
+      const int32_t *row = tpt + (size_t)tok * max_pages + key0 / P;
+      for (int j = 0; j < 8; ++j) pg[j] = j < npg ? row[j] : -1;
+      dec_start[4 * c + 2] = make_int4(pg[0], pg[1], pg[2], pg[3]);
+      dec_start[4 * c + 3] = make_int4(pg[4], pg[5], pg[6], pg[7]);
     }
     if (W > 0) {
       long long w = (long long)c * W / C;
