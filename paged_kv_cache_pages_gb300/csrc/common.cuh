@@ -20,7 +20,7 @@ namespace pa {
 //   flags          int  [T]      plan scratch: run-start flags
 //   runs           int  [T + 1]  plan scratch: first token of each run
 //   tile_off       int  [T + 1]  prefix sums of prefill work (key blocks x items) per tile
-//   dec_start      int4 [4C]     first decode unit of each CTA: (i, g, kb, token), (units, kv_len, -, -),
+//   dec_start      int4 [4C]     first decode unit of each CTA: (i, g, kb, token), (units, kv_len, first block of i, -),
 //                                  then the page ids of that unit's key block (8 ints, -1 past its end)
 //   pf_start       int4 [C]      first prefill unit of each CTA: (tile, item in tile, kb, -)
 //   pf_cnt         int  [T * Hkv * NP * 2 * 4]  arrival counters of split prefill items,

@@ -42,6 +42,8 @@ constexpr float kDecRescale = 8.0f;                // lazy max: rescale when it 
 constexpr int kBox = KB * 128;                     // one 128-row x 64-dim swizzled box (16 KB)
 static_assert(kKeysPerWarp == 16, "warp key slice is 16 rows");
 
+constexpr int kBarBytes = 1024;  // barriers, stage metadata, jobs, flags
+
 template <int D, int G>
 struct DecCfg {
   static constexpr int kHalves = D / 64;
@@ -50,29 +52,51 @@ struct DecCfg {
   static constexpr int kStage = 2 * kBlk + kQ;                // multiple of 1024
   static constexpr int kMergeDims = 64;                       // the warps merge 64 dims at a time
   static constexpr int kMerge = kDecWarps * G * (kMergeDims + 2) * 4;
-  static constexpr int kFixed = kMerge + 512;                 // + barriers, jobs, flags
+  static constexpr int kPart = G * (D + 2) * 4;               // one split partial (m, l, acc)
+  static constexpr int kBase = kMerge + kPart + kBarBytes;    // + own partial, barriers, jobs
   static constexpr int kBudget = 227 * 1024 - 2048;           // minus alignment slack
-  static constexpr int NS0 = (kBudget - kFixed) / kStage;
+  static constexpr int NS0 = (kBudget - kBase) / kStage;
   static constexpr int NS = NS0 > 6 ? 6 : NS0;
   static_assert(NS >= 2, "at least two stages");
+  // what the stages leave holds the other CTAs' partials of the final segment
+  static constexpr int kPref0 = (kBudget - kBase - NS * kStage) / kPart;
+  static constexpr int kPref = kPref0 > 7 ? 7 : kPref0;
+  static constexpr int kFixed = kBase + kPref * kPart;
   static constexpr int kSmem = NS * kStage + kFixed + 1024;
 };
 
 constexpr int kJobs = 4;  // hand-off ring from the consumers to the combining warp
 
 struct DecJob {
-  int ig, tok, g, c_first, c_last;  // ig < 0: no more jobs
-  int pad[3];
+  int ig, tok, g;  // ig < 0: no more jobs
+  int c_first, n_parts;  // the segment's parts (SegParts)
+  int fetch;             // 1: fetch the other parts of the final segment
+  int pad[2];
+};
+
+// What the producer tells the consumers about the unit a stage holds.
+struct StageMeta {
+  int rows;       // valid keys of the block (0: skip the block)
+  int i, g, kb;   // decode token index, KV head, key block
+  int units;      // key blocks of token i
+  int tok;        // ubatch token
+  int seg_begin;  // global unit index of the first block of (i, g)
+  int pad;
 };
 
 struct DecBars {
   uint64_t full[6], empty[6];
   uint64_t job_full[kJobs], job_empty[kJobs];
   DecJob jobs[kJobs];
-  int rows[6];  // valid keys of the block held by each stage (0: skip the block)
+  uint64_t fetched;  // the combining warp answered the fetch of the final segment's parts
+  StageMeta meta[6];
   int abort;
   int last;     // the consumers complete the split of the CTA's final segment
+  int fetch_ok; // 1: every other part of the final segment sits in the fetch area
+  int tail;     // the consumers reached the end of the final segment
 };
+
+static_assert(sizeof(DecBars) <= kBarBytes, "barrier area");
 
 // Position in the unit sequence of this CTA.
 struct UnitIt {
@@ -82,6 +106,7 @@ struct UnitIt {
   int units;  // key blocks of token i
   int tok;    // ubatch token
   int L;      // kv_len of the token (clamped to the row capacity)
+  int uoff;   // first key block of token i among the decode tokens' blocks
 };
 
 struct DecView {
@@ -95,7 +120,8 @@ struct DecView {
 
 __device__ __forceinline__ void it_token(UnitIt &it, int i, const DecView &v) {
   it.i = i;
-  it.units = v.tok_unit_off[i + 1] - v.tok_unit_off[i];
+  it.uoff = v.tok_unit_off[i];
+  it.units = v.tok_unit_off[i + 1] - it.uoff;
   it.tok = v.dec_tok[i];
   int L = v.kv[it.tok];
   it.L = min(max(L, 0), v.cap);
@@ -110,6 +136,7 @@ __device__ __forceinline__ void it_start(UnitIt &it, int4 s0, int4 s1) {
   it.tok = s0.w;
   it.units = s1.x;
   it.L = s1.y;
+  it.uoff = s1.z;
 }
 
 __device__ __forceinline__ void it_next(UnitIt &it, const DecView &v) {
@@ -145,6 +172,47 @@ __device__ __forceinline__ bool dec_wait(uint64_t *bar, uint32_t parity, int *er
 // Barrier of the consumer warps only (the producer warpgroup never joins).
 __device__ __forceinline__ void consumers_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kDecWarps * 32) : "memory");
+}
+
+// Arrival counters of split segments: a part is published by a release increment
+// after its partial is written; whoever sees every other part published reads them.
+__device__ __forceinline__ int ld_acquire(const int *p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ int atom_add_acq_rel(int *p, int x) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(x)
+               : "memory");
+  return old;
+}
+
+// Fold one partial (mp, lp, op) into the running (M, L, O) of two output dims of one
+// head.  Every combine path applies this arithmetic to the parts in CTA order, so the
+// result does not depend on which CTA or warp happens to do the combine.
+__device__ __forceinline__ void fold_pair(float &M, float &L, float2 &O, float mp, float lp,
+                                          float2 op) {
+  const float Mn = fmaxf(M, mp);
+  const float fo = M == -INFINITY ? 0.f : exp2_approx(M - Mn);
+  const float fp = mp == -INFINITY ? 0.f : exp2_approx(mp - Mn);
+  L = __fmaf_rn(lp, fp, __fmul_rn(L, fo));
+  O.x = __fmaf_rn(op.x, fp, __fmul_rn(O.x, fo));
+  O.y = __fmaf_rn(op.y, fp, __fmul_rn(O.y, fo));
+  M = Mn;
+}
+
+// The parts of a split segment (global units [ub, ue)) in CTA order: every CTA owns
+// at least one unit, so they are CTAs c_first, c_first + 1, ..., c_first + n - 1.
+struct SegParts {
+  int c_first;  // CTA of the segment's first unit
+  int n;        // number of parts
+};
+__device__ __forceinline__ SegParts seg_parts(int ub, int ue, int U, int C) {
+  SegParts sp;
+  sp.c_first = cta_of_unit(ub, U, C);
+  sp.n = cta_of_unit(ue - 1, U, C) - sp.c_first + 1;
+  return sp;
 }
 
 // ---- warp-level tensor path helpers ---------------------------------------------
@@ -193,6 +261,9 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
   unsigned char *ring = smem;
   float *merge = reinterpret_cast<float *>(smem + NS * Cfg::kStage);
   DecBars *bars = reinterpret_cast<DecBars *>(smem + NS * Cfg::kStage + Cfg::kMerge);
+  // this CTA's partial of its final segment, then the other CTAs' partials of it
+  float *own = reinterpret_cast<float *>(smem + NS * Cfg::kStage + Cfg::kMerge + kBarBytes);
+  float *pref = own + G * (D + 2);
 
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   if (tid == 0) {
@@ -204,7 +275,10 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
       mbar_init(&bars->job_full[j], 1);
       mbar_init(&bars->job_empty[j], 1);
     }
+    mbar_init(&bars->fetched, 1);
     bars->abort = 0;
+    bars->fetch_ok = 0;
+    bars->tail = 0;
     fence_mbar_init();
   }
   if (w == kDecWarps && lane == 0) {
@@ -228,13 +302,16 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
   int *dec_cnt = reinterpret_cast<int *>(a.ws + a.lay.dec_cnt);
 
   const int U = hdr->n_units;
-  const int C = gridDim.x, c = blockIdx.x;
+  const int c = blockIdx.x;
   // decode tokens with no key (kv_len 0) own no unit: their rows are zero
-  for (int i = c; i < v.n_dec; i += C) {
+  for (int i = c; i < v.n_dec; i += gridDim.x) {
     if (v.tok_unit_off[i + 1] != v.tok_unit_off[i]) continue;
     uint16_t *orow = a.out + (size_t)v.dec_tok[i] * a.Hq * D;
     for (int x = threadIdx.x; x < a.Hq * D; x += blockDim.x) orow[x] = 0;
   }
+  // the units go to C = min(gridDim.x, U) CTAs, each of which owns at least one
+  const int C = min((int)gridDim.x, U);
+  if (c >= C) return;
   const int u0 = (int)((int64_t)c * U / C), u1 = (int)((int64_t)(c + 1) * U / C);
   if (u0 >= u1) return;
   const int n = u1 - u0;
@@ -288,7 +365,16 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
           ys[j] = (j < npg && !bad) ? (page * a.Hkv + pit.g) * a.P : oob_row;
         }
         const bool seg_first = (k == 0) || pit.kb == 0;
-        bars->rows[st] = rows;
+        {
+          StageMeta &m = bars->meta[st];
+          m.rows = rows;
+          m.i = pit.i;
+          m.g = pit.g;
+          m.kb = pit.kb;
+          m.units = pit.units;
+          m.tok = pit.tok;
+          m.seg_begin = a.Hkv * pit.uoff + pit.g * pit.units;
+        }
         const uint32_t qbytes = seg_first ? (uint32_t)(G * D * 2) : 0u;
         mbar_arrive_expect_tx(&bars->full[st], 2u * Cfg::kBlk + qbytes);
 #pragma unroll
@@ -321,9 +407,13 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
       }
     } else if (w == kDecWarps + 1) {
       // -------------------------------------------------------------- combining warp
-      // For each (i, g) this CTA left a partial of: count the arrival; the CTA whose
-      // part lands last combines all parts and writes the row.  Runs beside the
-      // consumers, so their next segment never waits on this.
+      // Jobs from the consumers, in order: (a) a split segment that ended inside the
+      // range: publish this CTA's part; if it was the last part to arrive, combine all
+      // parts and write the row.  Runs beside the consumers, so their next segment
+      // never waits on it.  (b) the final segment, when it is split: as soon as every
+      // other part is published, copy them into shared memory, so the consumers can
+      // finish the row at the end of the range with no global round trip.
+      volatile int *tail = &bars->tail;
       for (int j = 0;; ++j) {
         const int q = j % kJobs;
         if (!dec_wait(&bars->job_full[q], (j / kJobs) & 1, err, abort)) break;
@@ -331,28 +421,76 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->job_empty[q]);
         if (job.ig < 0) break;
-        int n_parts = 0;
-        for (int cc = job.c_first; cc <= job.c_last; ++cc)
-          n_parts += cta_has_units(cc, U, C) ? 1 : 0;
-        int old = 0;
-        if (lane == 0) {
-          __threadfence();  // the consumers' partial is visible before the count
-          old = atomicAdd(&dec_cnt[job.ig], 1);
+        SegParts sp;
+        sp.c_first = job.c_first;
+        sp.n = job.n_parts;
+        const int n_parts = sp.n;
+        if (job.fetch) {
+          int ok = 0;
+          if (n_parts - 1 <= Cfg::kPref) {
+            // poll until the other parts are published or the consumers get there first
+            const uint64_t t0 = globaltimer_ns();
+            for (;;) {
+              int cnt = 0;
+              if (lane == 0) cnt = ld_acquire(&dec_cnt[job.ig]);
+              cnt = __shfl_sync(0xffffffffu, cnt, 0);
+              if (cnt == n_parts - 1) {
+                ok = 1;
+                break;
+              }
+              if (*tail || *abort || globaltimer_ns() - t0 > kWaitLimitNs) break;
+              __nanosleep(128);
+            }
+          }
+          if (ok) {
+            __syncwarp();  // lane 0's acquire orders every lane's reads below
+            // copy in float2 steps, a batch of loads in flight per part
+            constexpr int N2 = G * (D + 2) / 2;
+            constexpr int PER = (N2 + 31) / 32;
+            int slot = 0;
+            for (int jp = 0; jp < n_parts; ++jp) {
+              const int cc = sp.c_first + jp;
+              if (cc == c) continue;
+              const float2 *src =
+                  reinterpret_cast<const float2 *>(partials + (size_t)(job.ig + cc) * G * (D + 2));
+              float2 *dst = reinterpret_cast<float2 *>(pref + slot * G * (D + 2));
+              float2 t[PER];
+#pragma unroll
+              for (int r = 0; r < PER; ++r) {
+                const int x = lane + 32 * r;
+                t[r] = x < N2 ? __ldcg(src + x) : make_float2(0.f, 0.f);
+              }
+#pragma unroll
+              for (int r = 0; r < PER; ++r) {
+                const int x = lane + 32 * r;
+                if (x < N2) dst[x] = t[r];
+              }
+              ++slot;
+            }
+          }
+          __syncwarp();
+          if (lane == 0) {
+            bars->fetch_ok = ok;
+            mbar_arrive(&bars->fetched);
+          }
+          continue;
         }
+        int old = 0;
+        if (lane == 0) old = atom_add_acq_rel(&dec_cnt[job.ig], 1);
         old = __shfl_sync(0xffffffffu, old, 0);
         if (old != n_parts - 1) continue;
-        __threadfence();
-        // Online merge over the parts.  Lane owns outputs idx = lane + 32 t; per part,
-        // lanes < G fetch (m, l) of head `lane` and broadcast them, and every lane
-        // issues all its accumulator loads before using any (one L2 round trip per
-        // part).  The parts were written by other SMs: read them past L1.
+        __syncwarp();  // lane 0's acquire orders every lane's reads below
+        // Online fold over the parts in CTA order.  Lane owns outputs idx = lane + 32 t;
+        // per part, lanes < G fetch (m, l) of head `lane` and broadcast the factors, and
+        // every lane issues all its accumulator loads before using any (one L2 round
+        // trip per part).  The parts were written by other SMs: read them past L1.
         constexpr int NOUT = G * D / 32;
         float O[NOUT];
 #pragma unroll
         for (int t = 0; t < NOUT; ++t) O[t] = 0.f;
         float Mh = -INFINITY, Lh = 0.f;  // lane h < G: running max / sum of head h
-        for (int cc = job.c_first; cc <= job.c_last; ++cc) {
-          if (!cta_has_units(cc, U, C)) continue;
+        for (int jp = 0; jp < n_parts; ++jp) {
+          const int cc = sp.c_first + jp;
           const float *base = partials + (size_t)(job.ig + cc) * G * (D + 2);
           float Op[NOUT];
 #pragma unroll
@@ -365,17 +503,18 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
             mp = __ldcg(base + lane * (D + 2));
             lp = __ldcg(base + lane * (D + 2) + 1);
           }
+          // the same arithmetic as fold_pair, with the factors shared across a head
           const float Mn = fmaxf(Mh, mp);
           const float fo = Mh == -INFINITY ? 0.f : exp2_approx(Mh - Mn);
           const float fp = mp == -INFINITY ? 0.f : exp2_approx(mp - Mn);
-          Lh = Lh * fo + lp * fp;
+          Lh = __fmaf_rn(lp, fp, __fmul_rn(Lh, fo));
           Mh = Mn;
 #pragma unroll
           for (int t = 0; t < NOUT; ++t) {
             const int h = (lane + 32 * t) / D;
             const float a_o = __shfl_sync(0xffffffffu, fo, h);
             const float a_p = __shfl_sync(0xffffffffu, fp, h);
-            O[t] = O[t] * a_o + Op[t] * a_p;
+            O[t] = __fmaf_rn(Op[t], a_p, __fmul_rn(O[t], a_o));
           }
         }
 #pragma unroll
@@ -399,34 +538,55 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
   const bool head_lane = hr < G;
   const int key_base = w * kKeysPerWarp;
 
-  UnitIt cit;
-  it_start(cit, start0, start1);
   int seg_begin = 0;
   uint32_t qa[KSTEPS][2];  // A fragments of Q: columns 2cq.. and 8+2cq.. of each k-step
   float o[NT][4];          // O accumulators (rows hr and hr + 8)
   float m_run = -INFINITY; // running max of head hr (log2 domain)
   float l_part = 0.f;      // this lane's share of the row sum of head hr
-  bool dead = false;
-  int n_jobs = 0;          // partials handed to the combining warp
+  int n_jobs = 0;          // jobs handed to the combining warp
+  SegParts fin = {0, 0};  // parts of a split final segment
 
   for (int k = 0; k < n; ++k) {
     const int st = k % NS;
     unsigned char *stage = ring + st * Cfg::kStage;
     const uint32_t sK = smem_u32(stage), sV = smem_u32(stage + Cfg::kBlk);
+    // every consumer warp sees the same outcome of this wait, so all leave together
+    if (!dec_wait(&bars->full[st], (k / NS) & 1, err, abort)) break;
+    const StageMeta cit = bars->meta[st];  // the unit this stage holds
+    const int rows = cit.rows;
     const bool seg_first = (k == 0) || cit.kb == 0;
     const bool seg_last = (k == n - 1) || cit.kb + 1 == cit.units;
-    if (!dead) dead = !dec_wait(&bars->full[st], (k / NS) & 1, err, abort);
-    const int rows = dead ? 0 : bars->rows[st];
 
     if (seg_first) {
-      seg_begin = a.Hkv * v.tok_unit_off[cit.i] + cit.g * cit.units;
+      seg_begin = cit.seg_begin;
+      const int seg_end = seg_begin + cit.units;
+      if (seg_end >= u1 && !(seg_begin >= u0 && seg_end <= u1)) {
+        // the range ends inside a segment split over CTAs: have the combining warp
+        // fetch the other parts while this one streams
+        fin = seg_parts(seg_begin, seg_end, U, C);
+        if (tid == 0) {
+          const int q = n_jobs % kJobs;
+          if (dec_wait(&bars->job_empty[q], ((n_jobs / kJobs) & 1) ^ 1, err, abort)) {
+            DecJob job;
+            job.ig = cit.i * a.Hkv + cit.g;
+            job.tok = cit.tok;
+            job.g = cit.g;
+            job.c_first = fin.c_first;
+            job.n_parts = fin.n;
+            job.fetch = 1;
+            bars->jobs[q] = job;
+            mbar_arrive(&bars->job_full[q]);
+          }
+        }
+        ++n_jobs;
+      }
       const uint16_t *qs = reinterpret_cast<const uint16_t *>(stage + 2 * Cfg::kBlk);
 #pragma unroll
       for (int ks = 0; ks < KSTEPS; ++ks) {
-        qa[ks][0] = (head_lane && !dead)
+        qa[ks][0] = head_lane
                         ? *reinterpret_cast<const uint32_t *>(qs + hr * D + ks * 16 + 2 * cq)
                         : 0u;
-        qa[ks][1] = (head_lane && !dead)
+        qa[ks][1] = head_lane
                         ? *reinterpret_cast<const uint32_t *>(qs + hr * D + ks * 16 + 8 + 2 * cq)
                         : 0u;
       }
@@ -513,7 +673,8 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
 
     if (seg_last) {
       // ---- merge the warps 64 dims at a time in the merge area; write the row out,
-      // or a partial that the combining warp will fold across CTAs
+      // or a partial: in global memory for the combining warp (a segment that ends
+      // inside the range), in shared memory for the final segment
       constexpr int MD = Cfg::kMergeDims < D ? Cfg::kMergeDims : D;
       float *mw = merge;                  // [warps][G]
       float *lw = mw + kDecWarps * G;     // [warps][G]
@@ -527,8 +688,10 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
       }
       const int seg_units = cit.units;
       const bool direct = seg_begin >= u0 && seg_begin + seg_units <= u1;
+      const bool final_split = !direct && k == n - 1;
       const int ig = cit.i * a.Hkv + cit.g;
       const int slot = ig + c;
+      float *part = final_split ? own : partials + (size_t)slot * G * (D + 2);
 #pragma unroll
       for (int d0 = 0; d0 < D; d0 += MD) {
         if (head_lane) {
@@ -559,79 +722,109 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
             a.out[((size_t)cit.tok * a.Hq + cit.g * G + h) * D + dd] =
                 __half_as_ushort(__float2half_rn(r));
           } else {
-            float *pp = partials + ((size_t)slot * G + h) * (D + 2);
+            float *pp = part + h * (D + 2);
             pp[2 + dd] = oo;
             if (dd == 0) { pp[0] = M; pp[1] = Ls; }
           }
         }
         consumers_sync();  // the merge area may be rewritten
       }
-      if (!direct && k == n - 1) {
-        // The CTA's final segment continues into the next CTA, which handled its part
-        // first, so this CTA is almost always the last to arrive; everyone else is
-        // done too, so the consumers fold the parts right here, all loads at once.
-        const int64_t ub = seg_begin, ue = ub + seg_units;
-        const int c_first = cta_of_unit(ub, U, C), c_last = cta_of_unit(ue - 1, U, C);
-        int n_parts = 0;
-        for (int cc = c_first; cc <= c_last; ++cc) n_parts += cta_has_units(cc, U, C) ? 1 : 0;
-        if (tid == 0) {
-          __threadfence();  // the partial of every consumer is visible before the count
-          bars->last = atomicAdd(&dec_cnt[ig], 1) == n_parts - 1;
-        }
-        consumers_sync();
-        if (bars->last) {
-          __threadfence();
-          for (int idx = tid; idx < G * D; idx += kDecWarps * 32) {
-            const int h = idx / D, dd = idx - h * D;
-            float M = -INFINITY, Ls = 0.f, oo = 0.f;
-            for (int c0 = c_first; c0 <= c_last; c0 += 8) {
-              float mp[8], lp[8], op[8];
+      if (final_split) {
+        // The CTA's final segment is split over CTAs.  The others usually finished
+        // their parts long ago (the next CTA starts its range with it) and the combining
+        // warp has already copied them here; then the row is finished from shared
+        // memory.  Otherwise publish this part; the last to arrive combines.
+        if (tid == 0) *reinterpret_cast<volatile int *>(&bars->tail) = 1;
+        if (dec_wait(&bars->fetched, 0, err, abort)) {
+          const bool fetched = *reinterpret_cast<volatile int *>(&bars->fetch_ok) != 0;
+          bool combine = fetched;
+          if (!fetched) {
+            float *dst = partials + (size_t)slot * G * (D + 2);
+            for (int x = tid; x < G * (D + 2); x += kDecWarps * 32) dst[x] = own[x];
+            consumers_sync();
+            if (tid == 0) bars->last = atom_add_acq_rel(&dec_cnt[ig], 1) == fin.n - 1;
+            consumers_sync();
+            combine = bars->last != 0;
+          }
+          if (combine) {
+            // thread -> pairs of output dims (one head); every load of a batch of 8
+            // parts, for all of the thread's pairs, is in flight before the first fold
+            constexpr int NPAIR = G * D / 2;
+            constexpr int ITERS = (NPAIR + kDecWarps * 32 - 1) / (kDecWarps * 32);
+            const int own_j = c - fin.c_first;
+            float M[ITERS], Ls[ITERS];
+            float2 oo[ITERS];
 #pragma unroll
-              for (int j = 0; j < 8; ++j) {  // issue every load of the batch first
-                const int cc = c0 + j;
-                const bool use = cc <= c_last && cta_has_units(cc, U, C);
-                const float *pp = partials + ((size_t)(ig + (use ? cc : c_first)) * G + h) * (D + 2);
-                mp[j] = use ? __ldcg(pp) : -INFINITY;
-                lp[j] = use ? __ldcg(pp + 1) : 0.f;
-                op[j] = use ? __ldcg(pp + 2 + dd) : 0.f;
-              }
-              float Mn = M;
-#pragma unroll
-              for (int j = 0; j < 8; ++j) Mn = fmaxf(Mn, mp[j]);
-              const float fo = M == -INFINITY ? 0.f : exp2_approx(M - Mn);
-              Ls *= fo;
-              oo *= fo;
+            for (int r = 0; r < ITERS; ++r) {
+              M[r] = -INFINITY;
+              Ls[r] = 0.f;
+              oo[r] = make_float2(0.f, 0.f);
+            }
+            for (int j0 = 0; j0 < fin.n; j0 += 8) {
+              const int nb = min(8, fin.n - j0);
+              const float *src[8];
 #pragma unroll
               for (int j = 0; j < 8; ++j) {
-                const float f = mp[j] == -INFINITY ? 0.f : exp2_approx(mp[j] - Mn);
-                Ls += f * lp[j];
-                oo += f * op[j];
+                const int jp = j0 + j;
+                if (jp == own_j || j >= nb) src[j] = own;
+                else if (fetched) src[j] = pref + (jp < own_j ? jp : jp - 1) * G * (D + 2);
+                else src[j] = partials + (size_t)(ig + fin.c_first + jp) * G * (D + 2);
               }
-              M = Mn;
+              float mp[ITERS][8], lp[ITERS][8];
+              float2 op[ITERS][8];
+#pragma unroll
+              for (int r = 0; r < ITERS; ++r) {
+                const int pair = tid + r * kDecWarps * 32;
+                const int pr = pair < NPAIR ? pair : 0;
+                const int h = (2 * pr) / D, dd = 2 * pr - h * D;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  const bool local = fetched || j0 + j == own_j || j >= nb;
+                  const float *pp = src[j] + h * (D + 2);
+                  const float2 *p2 = reinterpret_cast<const float2 *>(pp + 2 + dd);
+                  mp[r][j] = local ? pp[0] : __ldcg(pp);
+                  lp[r][j] = local ? pp[1] : __ldcg(pp + 1);
+                  op[r][j] = local ? *p2 : __ldcg(p2);
+                }
+              }
+#pragma unroll
+              for (int r = 0; r < ITERS; ++r)
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                  if (j < nb) fold_pair(M[r], Ls[r], oo[r], mp[r][j], lp[r][j], op[r][j]);
             }
-            a.out[((size_t)cit.tok * a.Hq + cit.g * G + h) * D + dd] =
-                __half_as_ushort(__float2half_rn(Ls > 0.f ? oo / Ls : 0.f));
+#pragma unroll
+            for (int r = 0; r < ITERS; ++r) {
+              const int pair = tid + r * kDecWarps * 32;
+              if (pair < NPAIR) {
+                const int h = (2 * pair) / D, dd = 2 * pair - h * D;
+                const float r0 = Ls[r] > 0.f ? oo[r].x / Ls[r] : 0.f;
+                const float r1 = Ls[r] > 0.f ? oo[r].y / Ls[r] : 0.f;
+                *reinterpret_cast<__half2 *>(a.out + ((size_t)cit.tok * a.Hq + cit.g * G + h) * D +
+                                             dd) = __floats2half2_rn(r0, r1);
+              }
+            }
+            if (tid == 0) dec_cnt[ig] = 0;  // ready for the next run of this plan
           }
-          if (tid == 0) dec_cnt[ig] = 0;  // ready for the next run of this plan
         }
       } else if (!direct && tid == 0) {
         // hand the cross-CTA combine to the combining warp
         const int q = n_jobs % kJobs;
         if (dec_wait(&bars->job_empty[q], ((n_jobs / kJobs) & 1) ^ 1, err, abort)) {
-          const int64_t ub = seg_begin, ue = ub + seg_units;
+          const SegParts sp = seg_parts(seg_begin, seg_begin + seg_units, U, C);
           DecJob job;
           job.ig = ig;
           job.tok = cit.tok;
           job.g = cit.g;
-          job.c_first = cta_of_unit(ub, U, C);
-          job.c_last = cta_of_unit(ue - 1, U, C);
+          job.c_first = sp.c_first;
+          job.n_parts = sp.n;
+          job.fetch = 0;
           bars->jobs[q] = job;
           mbar_arrive(&bars->job_full[q]);
         }
       }
-      if (!direct && k != n - 1) ++n_jobs;
+      if (!direct && !final_split) ++n_jobs;
     }
-    it_next(cit, v);
   }
   if (tid == 0) {  // no more jobs
     const int q = n_jobs % kJobs;

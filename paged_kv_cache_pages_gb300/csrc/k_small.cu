@@ -274,11 +274,13 @@ k_plan(const int32_t *__restrict__ tpt, int max_pages, const int32_t *__restrict
   if (tid == 0) tok_unit_off[dec_base] = unit_base;
   __syncthreads();
 
-  // 6. where each of the C CTAs starts in the decode and in the prefill work
+  // 6. where each of the C CTAs starts in the decode and in the prefill work.  The
+  // decode work goes to min(C, U) CTAs, so that each of them owns at least one unit.
   const long long U = (long long)unit_base * Hkv, W = work_base;
+  const int Cd = U < C ? (int)U : C;
   for (int c = tid; c < C; c += kPlanThreads) {
-    if (U > 0) {
-      long long u = (long long)c * U / C;
+    if (c < Cd) {
+      long long u = (long long)c * U / Cd;
       int i = upper_index(tok_unit_off, dec_base, u, Hkv);
       if (i >= dec_base) i = dec_base - 1;
       int units = tok_unit_off[i + 1] - tok_unit_off[i];
@@ -292,7 +294,7 @@ k_plan(const int32_t *__restrict__ tpt, int max_pages, const int32_t *__restrict
       const int L = min(max(kv[tok], 0), cap);
       const int kb = units > 0 ? (int)(r - (long long)g * units) : 0;
       dec_start[4 * c] = make_int4(i, g, kb, tok);
-      dec_start[4 * c + 1] = make_int4(units, L, 0, 0);
+      dec_start[4 * c + 1] = make_int4(units, L, tok_unit_off[i], 0);
       // page ids of the first key block, so the first copy needs no table lookup
       int pg[8];
       const int key0 = kb * KB, npg = (min(KB, L - key0) + P - 1) / P;
