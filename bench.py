@@ -29,6 +29,30 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "decode KV GB/s + prefill TFLOP/s, Qwen3-8B-shape paged attn, 8×16K, 1 GB300"
+
+# DRAM bytes (read + write) per launch from ncu captures of the same workloads, with a
+# digest of the kernel's sources at capture time: a kernel changed since then reports
+# traffic null.  k_prefill: mean of the 65 launches of one 8x16K step (launch list of
+# `bench.py --steps 2 --warmup 3 --no-cpu-baseline`); k_decode: one decode_8seq launch
+# (`profile_case decode`, cold L2).  Summaries and commands: profiles/.
+TRAFFIC = {
+    "k_prefill": {"bytes": 639.5e6, "files": ["k_prefill.cu"], "digest": "54d1addaff1d640d"},
+    "k_decode": {"bytes": 86.26e6, "files": ["k_decode.cu"], "digest": "2c05d73581de79d7"},
+}
+_TRAFFIC_HEADERS = ["common.cuh", "tc.cuh", "tmap.cuh", "kernels.cuh"]
+
+
+def traffic_of(kernel: str):
+    """Recorded DRAM bytes per launch of `kernel`, or None if its sources changed."""
+    import hashlib
+    rec = TRAFFIC[kernel]
+    csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "paged_kv_cache_pages_gb300",
+                        "csrc")
+    h = hashlib.sha256()
+    for f in rec["files"] + _TRAFFIC_HEADERS:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return rec["bytes"] if h.hexdigest()[:16] == rec["digest"] else None
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 DECODE_LAYERS = 36
 
@@ -274,6 +298,33 @@ def time_steps(torch, fn, steps, warmup, world, per_launch=None):
     return total_ms, kern_ms
 
 
+def time_launches(torch, fn, n_pairs, steps, warmup, world):
+    """Average device time of the launches that fn brackets with its (start, end)
+    event pairs.  Preferred: the step is captured as a CUDA graph with the event
+    records as graph nodes, so the pairs time each kernel inside the same graph
+    replay as the timed step (no host launch gaps).  If this PyTorch cannot put
+    event records in a graph, the pairs are timed in an eager pass instead.
+    Returns (total ms over all pairs of all steps, how it was timed)."""
+    try:
+        pairs = [(torch.cuda.Event(enable_timing=True, external=True),
+                  torch.cuda.Event(enable_timing=True, external=True)) for _ in range(n_pairs)]
+        graph = capture_step(torch, lambda: fn(pairs))
+    except (TypeError, RuntimeError):
+        _, ms = time_steps(torch, fn, steps, warmup, world, per_launch=n_pairs)
+        return ms, "eager pass, event pairs around each launch"
+    for _ in range(warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    total = 0.0
+    for _ in range(steps):
+        graph.replay()
+        torch.cuda.synchronize()
+        total += sum(a.elapsed_time(b) for a, b in pairs)
+    barrier(world)
+    return total, "event-record nodes around each launch inside a CUDA graph of the step"
+
+
 def capture_step(torch, fn):
     """One step captured as a CUDA graph (the same launches, replayed without
     host launch overhead)."""
@@ -344,7 +395,7 @@ def run_ours(args):
     graph = capture_step(torch, pb.step)
     with ClockSampler(local) as clk:
         total_ms, _ = time_steps(torch, graph.replay, args.steps, args.warmup, world)
-        _, kern_ms = time_steps(torch, pb.step, args.steps, args.warmup, world, per_launch=n_ub)
+        kern_ms, kern_how = time_launches(torch, pb.step, n_ub, args.steps, args.warmup, world)
     clocks = clk.summary()
     t_step = max_over_ranks(total_ms / 1e3 / args.steps, world)
     value = aggregate(pb.flops, t_step, world) / 1e12
@@ -371,7 +422,7 @@ def run_ours(args):
     db = DecodeBench(pa, torch, dev, seed=args.seed)
     d_graph = capture_step(torch, db.step)
     d_total, _ = time_steps(torch, d_graph.replay, args.steps, args.warmup, world)
-    _, d_kern = time_steps(torch, db.step, args.steps, args.warmup, world, per_launch=db.layers)
+    d_kern, _ = time_launches(torch, db.step, db.layers, args.steps, args.warmup, world)
     d_step = max_over_ranks(d_total / 1e3 / args.steps, world)
     d_value = aggregate(db.bytes_per_layer * db.layers, d_step, world) / 1e9
     d_kt = d_kern / 1e3 / (args.steps * db.layers)
@@ -394,13 +445,11 @@ def run_ours(args):
         "roofline": {"bound": "tensor", "kernel": "k_prefill", "achieved": round(achieved, 2),
                      "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                      "peak_source": f"{peak_src} bf16 sustained (f16 dense rate = bf16)",
-                     "traffic": None},
+                     "traffic": traffic_of("k_prefill")},
         "e2e": {"value": round(aggregate(pb.flops, e2e_s, world) / 1e12, 3), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": pb.launches_per_step * args.steps,
-        "timing": "value: CUDA-graph replay of whole steps; roofline: per-launch CUDA events "
-                  "in a non-graph pass of the same steps, each step queued behind a "
-                  "device-side spin so that host launch rate does not enter",
+        "timing": "value: CUDA-graph replay of whole steps; roofline: " + kern_how,
         "clocks": clocks,
         "decode": {"workload": "decode_8seq", "value": round(d_value, 1), "unit": "GB/s",
                    "layers": db.layers, "kv_bytes_per_layer": db.bytes_per_layer,
@@ -409,7 +458,8 @@ def run_ours(args):
                    "roofline": {"bound": "hbm", "kernel": "k_decode",
                                 "achieved": round(d_ach, 1), "peak": hbm, "unit": "GB/s",
                                 "frac": round(d_ach / hbm, 4),
-                                "peak_source": f"{peak_src} hbm copy", "traffic": None}},
+                                "peak_source": f"{peak_src} hbm copy",
+                                "traffic": traffic_of("k_decode")}},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_prefill(pb.wl, budget_s=args.cpu_budget)

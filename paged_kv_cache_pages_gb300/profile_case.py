@@ -4,8 +4,10 @@
       one ubatch of the 8 x 16K prefill (default: a late one, long contexts):
       expand -> append -> plan -> prefill -> decode, R times.  Device memory:
       the 655 MB KV pool (larger than L2) plus one ubatch.
-  python -m paged_kv_cache_pages_gb300.profile_case decode [--reps R]
-      the 8-sequence decode layer: expand -> plan -> append -> decode.
+  python -m paged_kv_cache_pages_gb300.profile_case decode [--reps R] [--pools N]
+      the 8-sequence decode layer: expand -> plan -> append -> decode, over N
+      copies of the 82 MB pool used in turn (default 8: 660 MB, larger than L2,
+      so every call streams its pool from HBM).
 
 Prints the average time of the attention call (CUDA events) and exits 0.
 """
@@ -64,7 +66,7 @@ def prefill(ubatch: int, reps: int):
           f"{flops / ms / 1e9:.1f} TFLOP/s (prefill+decode calls)")
 
 
-def decode(reps: int):
+def decode(reps: int, n_pools: int):
     c = workloads.decode(0)
     dev = "cuda"
     spt = torch.from_numpy(c.seq_page_table()).to(dev)
@@ -78,11 +80,20 @@ def decode(reps: int):
     ws = pa.new_workspace(c.T, c.Hq, c.Hkv, c.d, dev)
     out = torch.empty_like(q)
     pa.plan(tpt, kv, c.Hq, c.Hkv, c.P, c.d, ws)
-    ms = _time(lambda: pa.decode(q, kp, vp, tpt, kv, c.scale, out, ws), reps)
+    pools = [(kp, vp)] + [(kp.clone(), vp.clone()) for _ in range(n_pools - 1)]
+    turn = [0]
+
+    def fn():
+        k_, v_ = pools[turn[0] % len(pools)]
+        turn[0] += 1
+        pa.decode(q, k_, v_, tpt, kv, c.scale, out, ws)
+
+    ms = _time(fn, reps)
     if pa.read_error(ws):
         raise SystemExit("device error word set")
     nbytes = float(c.seq_len.astype(np.int64).sum()) * c.Hkv * c.d * 4
-    print(f"decode: {ms * 1e3:.1f} us/call {nbytes / ms / 1e6:.1f} GB/s (L2-warm, one pool)")
+    print(f"decode: {ms * 1e3:.1f} us/call {nbytes / ms / 1e6:.1f} GB/s "
+          f"({len(pools)} pools in turn, eager launches)")
 
 
 def main():
@@ -90,11 +101,12 @@ def main():
     ap.add_argument("case", choices=["prefill", "decode"])
     ap.add_argument("--ubatch", type=int, default=48)
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--pools", type=int, default=8)
     a = ap.parse_args()
     if a.case == "prefill":
         prefill(a.ubatch, a.reps)
     else:
-        decode(a.reps)
+        decode(a.reps, a.pools)
 
 
 if __name__ == "__main__":
