@@ -286,8 +286,39 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
     tc::prefetch_tmap(&maps.v);
   }
   // Launched as a programmatic dependent of the append kernel: the launch and the
-  // setup above overlap its tail; nothing written by earlier kernels is read before here.
+  // setup above overlap its tail.  Before waiting for it, the producer thread asks L2
+  // for the CTA's first key blocks: the plan's start record and the page table were
+  // written by kernels that finished before the append began, and a prefetch changes
+  // no result (if the append writes into a block, L2 holds the new rows; if a record
+  // is stale, the prefetch is merely wasted).
+  if (w == kDecWarps && lane == 0) {
+    const int4 *srec = reinterpret_cast<const int4 *>(a.ws + a.lay.dec_start) + 4 * blockIdx.x;
+    const int4 s0 = srec[0], s1 = srec[1], p0 = srec[2], p1 = srec[3];
+    const int g = s0.y, kb = s0.z, tok = s0.w, units = s1.x;
+    const int ppb = KB / a.P;  // pages per key block
+    const int pg0[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+    // a CTA without units has no record: only in-range rows are looked up
+    const bool sane = tok >= 0 && tok < a.T && kb >= 0 && g >= 0 && g < a.Hkv;
+    for (int u = 0; sane && u < NS && kb + u < units; ++u) {
+      if ((kb + u + 1) * ppb > a.max_pages) break;
+      const int32_t *row = a.tpt + (size_t)tok * a.max_pages + (size_t)(kb + u) * ppb;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (j >= ppb) break;
+        const int page = u == 0 ? pg0[j] : row[j];
+        if (page < 0 || page >= a.num_pages) continue;
+        const int y = (page * a.Hkv + g) * a.P;
+        for (int hf = 0; hf < Cfg::kHalves; ++hf) {
+          tc::tma_prefetch_2d(&maps.k, hf * 64, y);
+          tc::tma_prefetch_2d(&maps.v, hf * 64, y);
+        }
+      }
+    }
+  }
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the next kernel in the stream may be scheduled onto SMs as this grid's CTAs leave
+  // them (a programmatically launched successor still waits for this grid to complete)
+  asm volatile("griddepcontrol.launch_dependents;");
   __syncthreads();
   WsHeader *hdr = reinterpret_cast<WsHeader *>(a.ws);
   int *err = &hdr->err;

@@ -27,6 +27,14 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int x, 
       : "memory");
 }
 
+// Bring a tile into L2 without writing shared memory (no barrier; out-of-range
+// coordinates fetch nothing).
+__device__ __forceinline__ void tma_prefetch_2d(const void *tmap, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+               ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y)
+               : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void *tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
