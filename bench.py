@@ -34,10 +34,13 @@ METRIC = "decode KV GB/s + prefill TFLOP/s, Qwen3-8B-shape paged attn, 8×16K, 1
 # digest of the kernel's sources at capture time: a kernel changed since then reports
 # traffic null.  k_prefill: mean of the 65 launches of one 8x16K step (launch list of
 # `bench.py --steps 2 --warmup 3 --no-cpu-baseline`); k_decode: one decode_8seq launch
-# (`profile_case decode`, cold L2).  Summaries and commands: profiles/.
+# (`profile_case decode`, cold L2); k_copy_pages: one launch of `profile_case copy`
+# (writes still in L2 at the end of the launch are not counted).  Summaries and
+# commands: profiles/.
 TRAFFIC = {
-    "k_prefill": {"bytes": 639.5e6, "files": ["k_prefill.cu"], "digest": "54d1addaff1d640d"},
+    "k_prefill": {"bytes": 676.1e6, "files": ["k_prefill.cu"], "digest": "d6b71aeae63528c1"},
     "k_decode": {"bytes": 86.35e6, "files": ["k_decode.cu"], "digest": "255512206199014d"},
+    "k_copy_pages": {"bytes": 488.0e6, "files": ["k_small.cu"], "digest": "aa9a77d695743686"},
 }
 _TRAFFIC_HEADERS = ["common.cuh", "tc.cuh", "tmap.cuh", "kernels.cuh"]
 
@@ -379,6 +382,45 @@ def cpu_baseline_prefill(wl, budget_s=12.0):
 
 # ----------------------------------------------------------------------------- arms
 
+def bench_copy_pages(pa, torch, dev, steps, warmup, world, hbm, with_cpu, seed=0):
+    """Page copy of copy-on-write forks: 512 random pages of a decode-shaped pool
+    (8 KV heads x 128 rows x d 128, K and V: 512 KB a page) copied to 512 other
+    pages per launch (256 MB read + 256 MB written, more than L2).  GB/s counts
+    bytes read + written, like the HBM copy peak."""
+    import workloads
+    N, Hkv, P, d, n = 1280, 8, 128, 128, 512
+    rng = np.random.default_rng(seed + 7000)
+    ids = rng.permutation(N).astype(np.int32)
+    src_h, dst_h = ids[:n].copy(), ids[n:2 * n].copy()
+    kp = torch.empty((N, Hkv, P, d), dtype=torch.float16, device=dev).normal_()
+    vp = torch.empty_like(kp).normal_()
+    src, dst = torch.from_numpy(src_h).to(dev), torch.from_numpy(dst_h).to(dev)
+    g = capture_step(torch, lambda: pa.copy_pages(src, dst, kp, vp))
+    total_ms, _ = time_steps(torch, g.replay, steps, warmup, world)
+    t = max_over_ranks(total_ms / 1e3 / steps, world)
+    nbytes = 2.0 * 2 * n * Hkv * P * d * 2  # K and V, read and written
+    gbs = aggregate(nbytes, t, world) / 1e9
+    res = {"workload": "fork_copy_512_pages", "value": round(gbs, 1), "unit": "GB/s",
+           "bytes_per_launch": nbytes,
+           "roofline": {"bound": "hbm", "kernel": "k_copy_pages", "achieved": round(gbs / world, 1),
+                        "peak": hbm, "unit": "GB/s", "frac": round(gbs / world / hbm, 4),
+                        "traffic": traffic_of("k_copy_pages")}}
+    if with_cpu:
+        import oracle
+        k_h = workloads.randn_f16(rng, (N, Hkv, P, d))
+        v_h = workloads.randn_f16(rng, (N, Hkv, P, d))
+        oracle.copy_pages(src_h, dst_h, k_h, v_h)
+        reps, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < 1.0:
+            oracle.copy_pages(src_h, dst_h, k_h, v_h)
+            reps += 1
+        secs = time.perf_counter() - t0
+        res["cpu_baseline"] = {"value": round(nbytes * reps / secs / 1e9, 2), "unit": "GB/s",
+                               "cores": 1, "kind": "oracle",
+                               "sample": f"the same 512 page pairs, {reps} copies in {secs:.1f} s"}
+    return res
+
+
 def run_ours(args):
     import torch
     world, rank, local = dist_setup()
@@ -476,6 +518,10 @@ def run_ours(args):
                                 "peak_source": f"{peak_src} hbm copy",
                                 "traffic": traffic_of("k_decode")}},
     }
+    # rows beyond the headline, same bar: page copy of copy-on-write forks
+    line["next"] = {"copy_pages": bench_copy_pages(
+        pa, torch, dev, args.steps, args.warmup, world, hbm,
+        with_cpu=rank == 0 and world == 1 and not args.no_cpu_baseline, seed=args.seed)}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_prefill(pb.wl, budget_s=args.cpu_budget)
     if rank == 0:

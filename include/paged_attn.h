@@ -200,6 +200,25 @@ int paged_attn_validate(const int32_t *tok_page_table, int max_pages, const int3
                         int T, int P, int num_pages, int *err, void *stream);
 
 /*
+ * Page copy for copy-on-write forks (CacheFlow page, section 核心架构 2: blocks
+ * shared by reference count; 核心架构 3: a block-copy kernel).  A forked sequence
+ * shares every full page of its parent and gets a private copy of the partly
+ * filled last page before it appends to it (see pa_pool_fork).
+ *
+ * Copies whole pages, every KV head, K and V: page dst[i] <- page src[i], i < n.
+ *   src, dst [n] int32 (device)     page ids
+ *   k_pages, v_pages [num_pages][Hkv][P][d] binary16 (in/out, 16-byte aligned)
+ *   err (device, optional, may be NULL): PA_ERR_PAGE_RANGE is OR-ed in for a
+ *       pair with an id outside [0, num_pages); that pair is skipped.
+ * The dst ids must be distinct and none may be among the src ids: the pairs are
+ * copied in parallel.  Bit copy in 16-byte units.  One launch; PA_EUNSUPPORTED
+ * if Hkv * P * d is not a multiple of 8.
+ */
+int paged_copy_pages(const int32_t *src, const int32_t *dst, int n, uint16_t *k_pages,
+                     uint16_t *v_pages, int num_pages, int Hkv, int P, int d, int *err,
+                     void *stream);
+
+/*
  * Synchronise `stream` and copy the workspace error word to *err_host (host
  * pointer).  Returns PA_OK if it is zero, PA_EDEVICE otherwise.
  */
@@ -237,6 +256,18 @@ int pa_pool_share(pa_page_pool *pool, const int32_t *pages, int n);
 int pa_pool_release(pa_page_pool *pool, const int32_t *pages, int n);
 /* Reference count of one page (0 = free), or PA_EINVAL. */
 int pa_pool_refcount(const pa_page_pool *pool, int32_t page);
+/*
+ * Copy-on-write fork of a sequence that holds n_tokens tokens in pages[0 ..
+ * ceil(n_tokens / P)) (host arrays).  The child shares the full pages (one more
+ * reference each).  If the last page is partly filled, the child gets a fresh
+ * page in its place and (*copy_src, *copy_dst) receive (parent's last page,
+ * fresh page): copy it with paged_copy_pages before either side appends into
+ * it.  out_pages (host, ceil(n_tokens / P) entries) receives the child's list.
+ * Returns the number of pages to copy (0 or 1), PA_EINVAL (bad arguments or a
+ * page not in use), or PA_ENOSPACE; on error nothing changes.
+ */
+int pa_pool_fork(pa_page_pool *pool, const int32_t *pages, int n_tokens, int P,
+                 int32_t *out_pages, int32_t *copy_src, int32_t *copy_dst);
 
 #ifdef __cplusplus
 }

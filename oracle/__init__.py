@@ -62,6 +62,9 @@ def _load():
                                                 c_int, c_int, c_int, c_int, c_int, c_int,
                                                 c_double, ctypes.c_void_p, c_int, f64p]
             lib.ref_paged_attention.restype = c_int
+            lib.ref_copy_pages.argtypes = [i32p, i32p, c_int, u16p, u16p, c_int, c_int, c_int,
+                                           c_int]
+            lib.ref_copy_pages.restype = c_int
             lib.ref_num_threads.argtypes = []
             lib.ref_num_threads.restype = c_int
             _lib = lib
@@ -112,6 +115,18 @@ def kv_append(k, v, slot_mapping, k_pages, v_pages):
     if rc != 0:
         raise ValueError("kv_append: slot beyond the pool")
     return k_pages, v_pages
+
+
+def copy_pages(src, dst, k_pages, v_pages):
+    """Page copy of a copy-on-write fork on host arrays: page dst[i] <- page src[i]
+    in both pools ([N][Hkv][P][d] uint16, updated in place).  Returns the number of
+    pairs skipped because an id is outside the pool."""
+    src = _c(src, np.int32)
+    dst = _c(dst, np.int32)
+    assert k_pages.flags.c_contiguous and v_pages.flags.c_contiguous
+    assert k_pages.dtype == np.uint16 and v_pages.dtype == np.uint16
+    N, Hkv, P, d = k_pages.shape
+    return int(_load().ref_copy_pages(src, dst, src.shape[0], k_pages, v_pages, N, Hkv, P, d))
 
 
 def paged_attention(q, k_pages, v_pages, tok_page_table, tok_kv_len, scale, tokens=None):

@@ -114,6 +114,32 @@ int ref_kv_append(const uint16_t *k, const uint16_t *v, const int64_t *slot_mapp
 }
 
 /*
+ * Page copy for a copy-on-write fork (CacheFlow page "CacheFlow：基于 llama.cpp 的
+ * 多请求 LLM 推理优化引擎", section 核心架构 2 and 3: blocks shared by reference
+ * count; a block-copy kernel makes a private copy before a shared, partly filled
+ * block is written).  For each pair i < n: page dst[i] of both pools receives the
+ * contents of page src[i] (all KV heads).  Bit copy, pairs in order.  A pair with
+ * an id outside [0, num_pages) is skipped; returns the number of skipped pairs.
+ */
+int ref_copy_pages(const int32_t *src, const int32_t *dst, int n, uint16_t *k_pages,
+                   uint16_t *v_pages, int num_pages, int Hkv, int P, int d)
+{
+    int skipped = 0;
+    size_t page = (size_t)Hkv * P * d;
+    for (int i = 0; i < n; ++i) {
+        if (src[i] < 0 || src[i] >= num_pages || dst[i] < 0 || dst[i] >= num_pages) {
+            ++skipped;
+            continue;
+        }
+        memcpy(k_pages + (size_t)dst[i] * page, k_pages + (size_t)src[i] * page,
+               page * sizeof(uint16_t));
+        memcpy(v_pages + (size_t)dst[i] * page, v_pages + (size_t)src[i] * page,
+               page * sizeof(uint16_t));
+    }
+    return skipped;
+}
+
+/*
  * Paged attention, by definition.  For each selected token t and query head h,
  * with L = tok_kv_len[t] and g = h / (Hq / Hkv):
  *   K_t[j] = k_pages[tok_page_table[t][j / P]][g][j % P][:]   (j < L), same for V

@@ -10,6 +10,7 @@ is no fallback.
 Entry points mirror include/paged_attn.h:
   expand_ubatch   per-token page-table / kv_len expansion + slot mapping
   kv_append       reshape-and-cache into the paged pool
+  copy_pages      page copy of a copy-on-write fork
   plan / prefill / decode / run / forward   the attention itself
   validate, read_error, set_prefill_min_run, workspace_size
   PagePool        host page allocator with reference-counted sharing
@@ -59,6 +60,8 @@ _SIGS = {
     "pa_pool_share": ([_vp, _vp, _i], _i),
     "pa_pool_release": ([_vp, _vp, _i], _i),
     "pa_pool_refcount": ([_vp, ctypes.c_int32], _i),
+    "pa_pool_fork": ([_vp, _vp, _i, _i, _vp, _vp, _vp], _i),
+    "paged_copy_pages": ([_vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _vp, _vp], _i),
 }
 for _name, (_args, _res) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -144,6 +147,19 @@ def kv_append(k, v, slot_mapping, k_pages, v_pages, err=None, stream=None):
     _check(_lib.paged_kv_append(_ptr(k), _ptr(v), _ptr(slot_mapping), T, _ptr(k_pages),
                                 _ptr(v_pages), N, Hkv, P, d, _ptr(err), _stream(stream)),
            "paged_kv_append")
+
+
+def copy_pages(src, dst, k_pages, v_pages, err=None, stream=None):
+    """Page copy of a copy-on-write fork: page dst[i] <- page src[i] in both pools."""
+    _req(src, torch.int32, "src")
+    _req(dst, torch.int32, "dst")
+    _req(k_pages, torch.float16, "k_pages")
+    _req(v_pages, torch.float16, "v_pages")
+    if src.shape != dst.shape:
+        raise ValueError("src and dst must have the same length")
+    N, Hkv, P, d = k_pages.shape
+    _check(_lib.paged_copy_pages(_ptr(src), _ptr(dst), src.shape[0], _ptr(k_pages), _ptr(v_pages),
+                                 N, Hkv, P, d, _ptr(err), _stream(stream)), "paged_copy_pages")
 
 
 def plan(tok_page_table, tok_kv_len, Hq, Hkv, P, d, workspace, stream=None):
@@ -258,3 +274,16 @@ class PagePool:
 
     def refcount(self, page: int) -> int:
         return int(_lib.pa_pool_refcount(self._h, int(page)))
+
+    def fork(self, pages, n_tokens: int, P: int):
+        """Copy-on-write fork of a sequence holding n_tokens tokens in `pages`.
+        Returns (child pages, (src, dst) page pair to copy, or None)."""
+        n = (int(n_tokens) + P - 1) // P
+        buf = (ctypes.c_int32 * max(n, 1))(*pages[:n])
+        out = (ctypes.c_int32 * max(n, 1))()
+        cs, cd = ctypes.c_int32(-1), ctypes.c_int32(-1)
+        st = _lib.pa_pool_fork(self._h, buf, int(n_tokens), int(P), out, ctypes.byref(cs),
+                               ctypes.byref(cd))
+        if st < 0:
+            raise PagedAttnError(st, "pa_pool_fork")
+        return [int(out[i]) for i in range(n)], ((int(cs.value), int(cd.value)) if st else None)

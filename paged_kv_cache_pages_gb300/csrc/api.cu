@@ -147,6 +147,24 @@ int paged_kv_append(const uint16_t *k, const uint16_t *v, const int64_t *slot_ma
   return launch_status(cudaGetLastError());
 }
 
+int paged_copy_pages(const int32_t *src, const int32_t *dst, int n, uint16_t *k_pages,
+                     uint16_t *v_pages, int num_pages, int Hkv, int P, int d, int *err,
+                     void *stream) {
+  if (n < 0 || num_pages < 0 || Hkv <= 0 || P <= 0 || d <= 0) return PA_EINVAL;
+  const long long page_halves = (long long)Hkv * P * d;
+  if (page_halves % 8 != 0) return PA_EUNSUPPORTED;
+  if (n == 0) return PA_OK;
+  if (!src || !dst || !k_pages || !v_pages) return PA_EINVAL;
+  if (!aligned16(k_pages) || !aligned16(v_pages)) return PA_EALIGN;
+  const long long units = page_halves / 8;
+  int bx = (int)std::min<long long>((units + 255) / 256, 64);
+  dim3 grid(bx, (unsigned)std::min(n, 65535));
+  k_copy_pages<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      src, dst, n, reinterpret_cast<uint4 *>(k_pages), reinterpret_cast<uint4 *>(v_pages),
+      num_pages, units, err);
+  return launch_status(cudaGetLastError());
+}
+
 size_t paged_attn_workspace_size(int T, int Hq, int Hkv, int d) {
   if (T < 0 || check_shape(Hq, Hkv, 16, d) != PA_OK) return 0;
   int C = sm_count();

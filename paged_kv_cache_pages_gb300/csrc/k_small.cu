@@ -45,6 +45,28 @@ __global__ void k_expand(const int32_t *__restrict__ seq_pt, int n_seq, int max_
 // Append.  One thread per 16-byte chunk of a (token, kv head) row; K and V in
 // the same thread.  Consecutive threads cover consecutive bytes of a row.
 // ---------------------------------------------------------------------------
+// Page copy for copy-on-write forks: blockIdx.y walks the pairs, the x threads the
+// 16-byte units of one page (K and V).
+__global__ void k_copy_pages(const int32_t *__restrict__ src, const int32_t *__restrict__ dst,
+                             int n, uint4 *__restrict__ kp, uint4 *__restrict__ vp,
+                             int num_pages, long long page_units, int *err) {
+  for (int pr = blockIdx.y; pr < n; pr += gridDim.y) {
+    const int s = src[pr], d = dst[pr];
+    if (s < 0 || s >= num_pages || d < 0 || d >= num_pages) {
+      if (err && blockIdx.x == 0 && threadIdx.x == 0) atomicOr(err, PA_ERR_PAGE_RANGE);
+      continue;
+    }
+    const uint4 *ks = kp + (size_t)s * page_units, *vs = vp + (size_t)s * page_units;
+    uint4 *kd = kp + (size_t)d * page_units, *vd = vp + (size_t)d * page_units;
+    for (long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x; u < page_units;
+         u += (long long)gridDim.x * blockDim.x) {
+      const uint4 a = ks[u], b = vs[u];
+      kd[u] = a;
+      vd[u] = b;
+    }
+  }
+}
+
 __global__ void k_append(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
                          const int64_t *__restrict__ slot, int T, uint4 *__restrict__ kp,
                          uint4 *__restrict__ vp, int num_pages, int Hkv, int P, int chunks_per_row,

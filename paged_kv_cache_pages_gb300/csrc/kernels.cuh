@@ -10,6 +10,8 @@ __global__ void k_expand(const int32_t *seq_pt, int n_seq, int max_pages, const 
                          int64_t *slot, int *err);
 __global__ void k_append(const uint4 *k, const uint4 *v, const int64_t *slot, int T, uint4 *kp,
                          uint4 *vp, int num_pages, int Hkv, int P, int chunks_per_row, int *err);
+__global__ void k_copy_pages(const int32_t *src, const int32_t *dst, int n, uint4 *kp, uint4 *vp,
+                             int num_pages, long long page_units, int *err);
 __global__ void k_validate(const int32_t *tpt, int max_pages, const int32_t *kv, int T, int P,
                            int num_pages, int *err);
 __global__ void k_plan_mark(const int32_t *tpt, int max_pages, int T, unsigned char *ws,

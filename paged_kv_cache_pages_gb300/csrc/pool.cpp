@@ -78,6 +78,30 @@ int pa_pool_release(pa_page_pool *pool, const int32_t *pages, int n) {
   return PA_OK;
 }
 
+int pa_pool_fork(pa_page_pool *pool, const int32_t *pages, int n_tokens, int P,
+                 int32_t *out_pages, int32_t *copy_src, int32_t *copy_dst) {
+  if (!pool || n_tokens < 0 || P <= 0 || !copy_src || !copy_dst) return PA_EINVAL;
+  const int n_pages = (n_tokens + P - 1) / P;
+  if (n_pages > 0 && (!pages || !out_pages)) return PA_EINVAL;
+  if (!valid_busy(pool, pages, n_pages)) return PA_EINVAL;
+  const int full = n_tokens / P;  // pages the child may share as they are
+  const bool partial = full < n_pages;
+  if (partial && pool->free_pages.empty()) return PA_ENOSPACE;
+  for (int i = 0; i < full; ++i) {
+    ++pool->refcount[pages[i]];
+    out_pages[i] = pages[i];
+  }
+  if (!partial) return 0;
+  auto it = pool->free_pages.begin();
+  const int32_t fresh = *it;
+  pool->free_pages.erase(it);
+  pool->refcount[fresh] = 1;
+  out_pages[full] = fresh;
+  *copy_src = pages[full];
+  *copy_dst = fresh;
+  return 1;
+}
+
 int pa_pool_refcount(const pa_page_pool *pool, int32_t page) {
   if (!pool || page < 0 || page >= static_cast<int32_t>(pool->refcount.size())) return PA_EINVAL;
   return pool->refcount[page];

@@ -9,7 +9,11 @@
       copies of the 82 MB pool used in turn (default 8: 660 MB, larger than L2,
       so every call streams its pool from HBM).
 
-Prints the average time of the attention call (CUDA events) and exits 0.
+  python -m paged_kv_cache_pages_gb300.profile_case copy [--reps R]
+      page copy of copy-on-write forks: 512 of 1280 pages (8 KV heads x 128 rows
+      x d 128, K and V) copied to 512 others per call.
+
+Prints the average time of the call (CUDA events) and exits 0.
 """
 import argparse
 import os
@@ -96,17 +100,33 @@ def decode(reps: int, n_pools: int):
           f"({len(pools)} pools in turn, eager launches)")
 
 
+def copy(reps: int):
+    dev = "cuda"
+    N, Hkv, P, d, n = 1280, 8, 128, 128, 512
+    rng = np.random.default_rng(7000)
+    ids = rng.permutation(N).astype(np.int32)
+    src = torch.from_numpy(ids[:n].copy()).to(dev)
+    dst = torch.from_numpy(ids[n:2 * n].copy()).to(dev)
+    kp = torch.empty((N, Hkv, P, d), dtype=torch.float16, device=dev).normal_()
+    vp = torch.empty_like(kp).normal_()
+    ms = _time(lambda: pa.copy_pages(src, dst, kp, vp), reps)
+    nbytes = 2.0 * 2 * n * Hkv * P * d * 2
+    print(f"copy_pages: {ms * 1e3:.1f} us/call {nbytes / ms / 1e6:.1f} GB/s (read + written)")
+
+
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["prefill", "decode"])
+    ap.add_argument("case", choices=["prefill", "decode", "copy"])
     ap.add_argument("--ubatch", type=int, default=48)
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--pools", type=int, default=8)
     a = ap.parse_args()
     if a.case == "prefill":
         prefill(a.ubatch, a.reps)
-    else:
+    elif a.case == "decode":
         decode(a.reps, a.pools)
+    else:
+        copy(a.reps)
 
 
 if __name__ == "__main__":
