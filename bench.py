@@ -421,6 +421,42 @@ def bench_copy_pages(pa, torch, dev, steps, warmup, world, hbm, with_cpu, seed=0
     return res
 
 
+def bench_unified_span(pa, torch, db, steps, warmup, world, hbm, paged_ms_per_layer):
+    """The unified-span baseline on the decode workload: the same 36 layers, each
+    pool seen as one span shared by the 8 sequences (every token streams the whole
+    pool, free cells included, under a per-cell mask), against the paged decode."""
+    import workloads
+    c = db.case
+    tpt, kv, cs, cp, ts, tp = workloads.span_view(c)
+    dev = db.q[0].device
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    tpt, kv, cs, cp, ts, tp = t(tpt), t(kv), t(cs), t(cp), t(ts), t(tp)
+    ws = pa.new_workspace(c.T, c.Hq, c.Hkv, c.d, dev)
+    out = torch.empty_like(db.q[0])
+
+    def step():
+        for l in range(db.layers):
+            kp, vp = db.pools[l]
+            pa.masked_decode(db.q[l], kp, vp, tpt, kv, c.scale, cs, cp, ts, tp, out, ws)
+
+    g = capture_step(torch, step)
+    total_ms, _ = time_steps(torch, g.replay, steps, warmup, world)
+    ms_layer = max_over_ranks(total_ms / steps / db.layers, world)
+    span_bytes = float(c.T) * c.num_pages * c.Hkv * c.P * c.d * 2 * 2  # K+V of the span, per token
+    if pa.read_error(ws):
+        raise RuntimeError("device error word set in the unified-span baseline")
+    gbs = span_bytes / (ms_layer / 1e3) / 1e9
+    return {"workload": "decode_8seq_unified_span", "unit": "GB/s", "value": round(gbs * world, 1),
+            "ms_per_layer": round(ms_layer, 4), "bytes_per_layer": span_bytes,
+            "paged_ms_per_layer": round(paged_ms_per_layer, 4),
+            "paged_speedup": round(ms_layer / paged_ms_per_layer, 2),
+            "bytes_ratio": round(span_bytes / db.bytes_per_layer, 2),
+            "roofline": {"bound": "hbm", "kernel": "k_decode (masked)", "achieved": round(gbs, 1),
+                         "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4),
+                         "traffic": None},
+            "timing": "CUDA graph of 36 layers, each a plan + masked decode launch"}
+
+
 def run_ours(args):
     import torch
     world, rank, local = dist_setup()
@@ -519,9 +555,13 @@ def run_ours(args):
                                 "traffic": traffic_of("k_decode")}},
     }
     # rows beyond the headline, same bar: page copy of copy-on-write forks
-    line["next"] = {"copy_pages": bench_copy_pages(
-        pa, torch, dev, args.steps, args.warmup, world, hbm,
-        with_cpu=rank == 0 and world == 1 and not args.no_cpu_baseline, seed=args.seed)}
+    line["next"] = {
+        "copy_pages": bench_copy_pages(
+            pa, torch, dev, args.steps, args.warmup, world, hbm,
+            with_cpu=rank == 0 and world == 1 and not args.no_cpu_baseline, seed=args.seed),
+        "unified_span": bench_unified_span(pa, torch, db, args.steps, args.warmup, world, hbm,
+                                           d_kt * 1e3),
+    }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_prefill(pb.wl, budget_s=args.cpu_budget)
     if rank == 0:

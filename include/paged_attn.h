@@ -200,6 +200,32 @@ int paged_attn_validate(const int32_t *tok_page_table, int max_pages, const int3
                         int T, int P, int num_pages, int *err, void *stream);
 
 /*
+ * Unified-span baseline (UA-PagedAttention page, section 作品简介: the original
+ * llama.cpp cache is one span of cells shared by all sequences, and attention
+ * reads the whole span under a mask that keeps each query's own sequence).
+ * Split-KV decode attention of every token over the keys its table row names,
+ * keeping only key j whose slot s = page * P + j % P holds a cell of the token's
+ * own sequence at a position up to its own:
+ *     cell_seq[s] == tok_seq[t]  and  cell_pos[s] <= tok_pos[t].
+ * Point every token's row at all pages of a span, with kv_len = the span length,
+ * and this is the unified-cache attention that paging replaces: same kernel
+ * engine as paged_attn_decode, but each token streams the whole span.
+ *   cell_seq, cell_pos [num_pages * P] int32 (device, 16-byte aligned): the
+ *       sequence (-1 = free) and position of the cell in each slot
+ *   tok_seq, tok_pos [T] int32 (device): each token's sequence and position
+ *   other arguments as paged_attn_forward.  Plans on its own (every token goes
+ *   to the split-KV path) and writes out for every token.  A token whose mask
+ *   keeps no key gets a zero row.
+ */
+int paged_attn_masked_decode(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
+                             const int32_t *tok_page_table, int max_pages,
+                             const int32_t *tok_kv_len, int T, int Hq, int Hkv, int P, int d,
+                             int num_pages, float scale, const int32_t *cell_seq,
+                             const int32_t *cell_pos, const int32_t *tok_seq,
+                             const int32_t *tok_pos, uint16_t *out, void *workspace,
+                             size_t workspace_bytes, void *stream);
+
+/*
  * Page copy for copy-on-write forks (CacheFlow page, section 核心架构 2: blocks
  * shared by reference count; 核心架构 3: a block-copy kernel).  A forked sequence
  * shares every full page of its parent and gets a private copy of the partly

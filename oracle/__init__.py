@@ -65,6 +65,11 @@ def _load():
             lib.ref_copy_pages.argtypes = [i32p, i32p, c_int, u16p, u16p, c_int, c_int, c_int,
                                            c_int]
             lib.ref_copy_pages.restype = c_int
+            lib.ref_masked_attention.argtypes = [u16p, u16p, u16p, i32p, c_int, i32p,
+                                                 c_int, c_int, c_int, c_int, c_int, c_int,
+                                                 c_double, i32p, i32p, i32p, i32p,
+                                                 ctypes.c_void_p, c_int, f64p]
+            lib.ref_masked_attention.restype = c_int
             lib.ref_num_threads.argtypes = []
             lib.ref_num_threads.restype = c_int
             _lib = lib
@@ -155,4 +160,37 @@ def paged_attention(q, k_pages, v_pages, tok_page_table, tok_kv_len, scale, toke
                                      float(scale), sel, n, out)
     if rc != 0:
         raise ValueError("paged_attention: page id or kv_len out of range")
+    return out
+
+
+def masked_attention(q, k_pages, v_pages, tok_page_table, tok_kv_len, scale, cell_seq, cell_pos,
+                     tok_seq, tok_pos, tokens=None):
+    """fp64 attention over each token's table row, keeping only the slots that hold a
+    cell of the token's own sequence at a position up to its own (the unified-span
+    baseline).  cell_seq / cell_pos: [num_pages * P] int32.  Returns float64
+    [T or len(tokens)][Hq][d]."""
+    q = _c(q, np.uint16)
+    k_pages = _c(k_pages, np.uint16)
+    v_pages = _c(v_pages, np.uint16)
+    tpt = _c(tok_page_table, np.int32)
+    kv = _c(tok_kv_len, np.int32)
+    cs, cp = _c(cell_seq, np.int32), _c(cell_pos, np.int32)
+    ts, tp = _c(tok_seq, np.int32), _c(tok_pos, np.int32)
+    T, Hq, d = q.shape
+    N, Hkv, P, d2 = k_pages.shape
+    assert d2 == d and Hq % Hkv == 0 and cs.shape[0] >= N * P and cp.shape[0] >= N * P
+    max_pages = tpt.shape[1]
+    if tokens is None:
+        sel, n = None, T
+    else:
+        tok_arr = _c(tokens, np.int32)
+        n = tok_arr.shape[0]
+        sel = tok_arr.ctypes.data_as(ctypes.c_void_p)
+    out = np.zeros((n, Hq, d), np.float64)
+    if n == 0:
+        return out
+    rc = _load().ref_masked_attention(q, k_pages, v_pages, tpt, max_pages, kv, T, Hq, Hkv, P, d,
+                                      N, float(scale), cs, cp, ts, tp, sel, n, out)
+    if rc != 0:
+        raise ValueError("masked_attention: page id or kv_len out of range")
     return out

@@ -209,6 +209,77 @@ int ref_paged_attention(const uint16_t *q, const uint16_t *k_pages, const uint16
     return bad ? -1 : 0;
 }
 
+/*
+ * Masked attention over a shared span of cells, the baseline that paging replaces
+ * (UA-PagedAttention page, section 作品简介: the original cache is one span shared
+ * by all sequences and attention reads all of it under a mask).  As
+ * ref_paged_attention, except that key j (slot s = page * P + j % P of the token's
+ * row) is used only if cell_seq[s] == tok_seq[t] and cell_pos[s] <= tok_pos[t];
+ * the softmax runs over the kept keys; a token that keeps none gets a zero row.
+ * Keys are gathered with their mask first, then the softmax is computed.
+ */
+int ref_masked_attention(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
+                         const int32_t *tok_page_table, int max_pages, const int32_t *tok_kv_len,
+                         int T, int Hq, int Hkv, int P, int d, int num_pages, double scale,
+                         const int32_t *cell_seq, const int32_t *cell_pos,
+                         const int32_t *tok_seq, const int32_t *tok_pos,
+                         const int32_t *tokens, int n_tok, double *out)
+{
+    int G = Hq / Hkv;
+    int n = tokens ? n_tok : T;
+    int bad = 0;
+    long long pairs = (long long)n * Hq;
+#pragma omp parallel for schedule(dynamic, 1) reduction(|: bad)
+    for (long long pi = 0; pi < pairs; ++pi) {
+        int ti = (int)(pi / Hq), h = (int)(pi % Hq);
+        int t = tokens ? tokens[ti] : ti;
+        int g = h / G;
+        int L = tok_kv_len[t];
+        double *o = out + ((size_t)ti * Hq + h) * d;
+        for (int i = 0; i < d; ++i) o[i] = 0.0;
+        if (L <= 0) continue;
+        if (L > max_pages * P) { bad = 1; continue; }
+        double *Kt = (double *)malloc(sizeof(double) * (size_t)L * d);
+        double *Vt = (double *)malloc(sizeof(double) * (size_t)L * d);
+        double *s = (double *)malloc(sizeof(double) * (size_t)L);
+        const int32_t *row = tok_page_table + (size_t)t * max_pages;
+        int kept = 0, ok = 1;
+        /* gather the kept keys and values of this token */
+        for (int j = 0; j < L && ok; ++j) {
+            int page = row[j / P];
+            if (page < 0 || page >= num_pages) { ok = 0; break; }
+            size_t slot = (size_t)page * P + (j % P);
+            if (cell_seq[slot] != tok_seq[t] || cell_pos[slot] > tok_pos[t]) continue;
+            size_t base = (((size_t)page * Hkv + g) * P + (j % P)) * d;
+            for (int i = 0; i < d; ++i) {
+                Kt[(size_t)kept * d + i] = ref_f16_to_f64(k_pages[base + i]);
+                Vt[(size_t)kept * d + i] = ref_f16_to_f64(v_pages[base + i]);
+            }
+            ++kept;
+        }
+        if (!ok) {
+            bad = 1;
+        } else if (kept > 0) {
+            const uint16_t *qh = q + ((size_t)t * Hq + h) * d;
+            double m = -INFINITY;
+            for (int j = 0; j < kept; ++j) {
+                double acc = 0.0;
+                for (int i = 0; i < d; ++i) acc += ref_f16_to_f64(qh[i]) * Kt[(size_t)j * d + i];
+                s[j] = scale * acc;
+                if (s[j] > m) m = s[j];
+            }
+            double Z = 0.0;
+            for (int j = 0; j < kept; ++j) { s[j] = exp(s[j] - m); Z += s[j]; }
+            for (int j = 0; j < kept; ++j) {
+                double w = s[j] / Z;
+                for (int i = 0; i < d; ++i) o[i] += w * Vt[(size_t)j * d + i];
+            }
+        }
+        free(Kt); free(Vt); free(s);
+    }
+    return bad ? -1 : 0;
+}
+
 /* Number of threads the OpenMP runtime will use (reported beside CPU timings). */
 int ref_num_threads(void)
 {

@@ -11,6 +11,7 @@ Entry points mirror include/paged_attn.h:
   expand_ubatch   per-token page-table / kv_len expansion + slot mapping
   kv_append       reshape-and-cache into the paged pool
   copy_pages      page copy of a copy-on-write fork
+  masked_decode   the unified-span baseline (masked attention over a shared span)
   plan / prefill / decode / run / forward   the attention itself
   validate, read_error, set_prefill_min_run, workspace_size
   PagePool        host page allocator with reference-counted sharing
@@ -62,6 +63,8 @@ _SIGS = {
     "pa_pool_refcount": ([_vp, ctypes.c_int32], _i),
     "pa_pool_fork": ([_vp, _vp, _i, _i, _vp, _vp, _vp], _i),
     "paged_copy_pages": ([_vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _vp, _vp], _i),
+    "paged_attn_masked_decode": ([_vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i,
+                                  ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i),
 }
 for _name, (_args, _res) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -147,6 +150,28 @@ def kv_append(k, v, slot_mapping, k_pages, v_pages, err=None, stream=None):
     _check(_lib.paged_kv_append(_ptr(k), _ptr(v), _ptr(slot_mapping), T, _ptr(k_pages),
                                 _ptr(v_pages), N, Hkv, P, d, _ptr(err), _stream(stream)),
            "paged_kv_append")
+
+
+def masked_decode(q, k_pages, v_pages, tok_page_table, tok_kv_len, scale, cell_seq, cell_pos,
+                  tok_seq, tok_pos, out, workspace, stream=None):
+    """Unified-span baseline: split-KV attention of every token over its row, keeping
+    only the slots whose cell belongs to the token's sequence at a position up to its
+    own.  Plans on its own."""
+    for t, n in ((q, "q"), (k_pages, "k_pages"), (v_pages, "v_pages"), (out, "out")):
+        _req(t, torch.float16, n)
+    for t, n in ((tok_page_table, "tok_page_table"), (tok_kv_len, "tok_kv_len"),
+                 (cell_seq, "cell_seq"), (cell_pos, "cell_pos"), (tok_seq, "tok_seq"),
+                 (tok_pos, "tok_pos")):
+        _req(t, torch.int32, n)
+    T, Hq, d = q.shape
+    N, Hkv, P, _ = k_pages.shape
+    max_pages = tok_page_table.shape[1]
+    _check(_lib.paged_attn_masked_decode(
+        _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(tok_page_table), max_pages, _ptr(tok_kv_len),
+        T, Hq, Hkv, P, d, N, float(scale), _ptr(cell_seq), _ptr(cell_pos), _ptr(tok_seq),
+        _ptr(tok_pos), _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)),
+        "paged_attn_masked_decode")
+    return out
 
 
 def copy_pages(src, dst, k_pages, v_pages, err=None, stream=None):

@@ -86,6 +86,7 @@ AttnArgs make_args(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v
   a.D = d;
   a.num_pages = num_pages;
   a.scale_log2 = scale * kLog2e;
+  a.cell_seq = a.cell_pos = a.tok_seq = a.tok_pos = nullptr;
   return a;
 }
 
@@ -172,9 +173,9 @@ size_t paged_attn_workspace_size(int T, int Hq, int Hkv, int d) {
   return ws_layout(T, Hq, Hkv, d, C).total;
 }
 
-int paged_attn_plan(const int32_t *tok_page_table, int max_pages, const int32_t *tok_kv_len,
-                    int T, int Hq, int Hkv, int P, int d, void *workspace, size_t workspace_bytes,
-                    void *stream) {
+static int plan_with(const int32_t *tok_page_table, int max_pages, const int32_t *tok_kv_len,
+                     int T, int Hq, int Hkv, int P, int d, void *workspace,
+                     size_t workspace_bytes, void *stream, int min_run) {
   int st = check_attn(nullptr, nullptr, nullptr, tok_page_table, max_pages, tok_kv_len, T, Hq, Hkv,
                       P, d, 1, nullptr, workspace, workspace_bytes, false);
   if (st != PA_OK) return st;
@@ -183,7 +184,6 @@ int paged_attn_plan(const int32_t *tok_page_table, int max_pages, const int32_t 
   WsLayout lay = ws_layout(T, Hq, Hkv, d, C);
   const int G = Hq / Hkv;
   const int NP = G >= 2 ? G / 2 : 1;
-  int min_run = g_min_run.load();
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   unsigned char *ws = static_cast<unsigned char *>(workspace);
   int blocks = (T + 7) / 8;
@@ -193,6 +193,41 @@ int paged_attn_plan(const int32_t *tok_page_table, int max_pages, const int32_t 
   k_plan<<<1, 1024, 0, s>>>(tok_page_table, max_pages, tok_kv_len, T, P, Hkv, NP, min_run, C, ws,
                             lay);
   return launch_status(cudaGetLastError());
+}
+
+int paged_attn_plan(const int32_t *tok_page_table, int max_pages, const int32_t *tok_kv_len,
+                    int T, int Hq, int Hkv, int P, int d, void *workspace, size_t workspace_bytes,
+                    void *stream) {
+  return plan_with(tok_page_table, max_pages, tok_kv_len, T, Hq, Hkv, P, d, workspace,
+                   workspace_bytes, stream, g_min_run.load());
+}
+
+int paged_attn_masked_decode(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
+                             const int32_t *tok_page_table, int max_pages,
+                             const int32_t *tok_kv_len, int T, int Hq, int Hkv, int P, int d,
+                             int num_pages, float scale, const int32_t *cell_seq,
+                             const int32_t *cell_pos, const int32_t *tok_seq,
+                             const int32_t *tok_pos, uint16_t *out, void *workspace,
+                             size_t workspace_bytes, void *stream) {
+  int st = check_attn(q, k_pages, v_pages, tok_page_table, max_pages, tok_kv_len, T, Hq, Hkv, P, d,
+                      num_pages, out, workspace, workspace_bytes, true);
+  if (st != PA_OK || T == 0) return st;
+  if (!cell_seq || !cell_pos || !tok_seq || !tok_pos) return PA_EINVAL;
+  if (!aligned16(cell_seq) || !aligned16(cell_pos)) return PA_EALIGN;
+  // every token on the split-KV path (the tensor-core tiles have no per-key mask)
+  st = plan_with(tok_page_table, max_pages, tok_kv_len, T, Hq, Hkv, P, d, workspace,
+                 workspace_bytes, stream, INT_MAX);
+  if (st != PA_OK) return st;
+  AttnArgs a = make_args(q, k_pages, v_pages, tok_page_table, max_pages, tok_kv_len, T, Hq, Hkv, P,
+                         d, num_pages, scale, out, workspace);
+  a.cell_seq = cell_seq;
+  a.cell_pos = cell_pos;
+  a.tok_seq = tok_seq;
+  a.tok_pos = tok_pos;
+  AttnMaps maps;
+  st = encode_attn_maps(a, &maps);
+  if (st != PA_OK) return st;
+  return launch_status(launch_decode(a, sm_count(), &maps, static_cast<cudaStream_t>(stream)));
 }
 
 int paged_attn_prefill(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,

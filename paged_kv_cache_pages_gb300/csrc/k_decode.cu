@@ -44,12 +44,13 @@ static_assert(kKeysPerWarp == 16, "warp key slice is 16 rows");
 
 constexpr int kBarBytes = 1024;  // barriers, stage metadata, jobs, flags
 
-template <int D, int G>
+template <int D, int G, bool MASK>
 struct DecCfg {
   static constexpr int kHalves = D / 64;
   static constexpr int kBlk = kHalves * kBox;                 // one block of K (or V)
   static constexpr int kQ = ((G * D * 2) + 1023) / 1024 * 1024;  // the group's query rows
-  static constexpr int kStage = 2 * kBlk + kQ;                // multiple of 1024
+  static constexpr int kCells = MASK ? 2 * KB * 4 : 0;        // (sequence, position) of each key
+  static constexpr int kStage = 2 * kBlk + kQ + kCells;       // multiple of 1024
   static constexpr int kMergeDims = 64;                       // the warps merge 64 dims at a time
   static constexpr int kMerge = kDecWarps * G * (kMergeDims + 2) * 4;
   static constexpr int kPart = G * (D + 2) * 4;               // one split partial (m, l, acc)
@@ -81,6 +82,7 @@ struct StageMeta {
   int units;      // key blocks of token i
   int tok;        // ubatch token
   int seg_begin;  // global unit index of the first block of (i, g)
+  int seq, pos;   // masked variant: the token's sequence and position
   int pad;
 };
 
@@ -107,6 +109,7 @@ struct UnitIt {
   int tok;    // ubatch token
   int L;      // kv_len of the token (clamped to the row capacity)
   int uoff;   // first key block of token i among the decode tokens' blocks
+  int seq, pos;  // masked variant: the token's sequence and position (else 0)
 };
 
 struct DecView {
@@ -116,6 +119,7 @@ struct DecView {
   int Hkv;
   int cap;
   const int32_t *kv;
+  const int32_t *tok_seq, *tok_pos;  // masked variant only, else null
 };
 
 __device__ __forceinline__ void it_token(UnitIt &it, int i, const DecView &v) {
@@ -125,11 +129,13 @@ __device__ __forceinline__ void it_token(UnitIt &it, int i, const DecView &v) {
   it.tok = v.dec_tok[i];
   int L = v.kv[it.tok];
   it.L = min(max(L, 0), v.cap);
+  it.seq = v.tok_seq ? v.tok_seq[it.tok] : 0;
+  it.pos = v.tok_pos ? v.tok_pos[it.tok] : 0;
 }
 
 // Iterator at the CTA's first unit, as placed by the planner: (i, g, kb, token) and
 // (units, kv_len) -- no dependent loads before the first copy.
-__device__ __forceinline__ void it_start(UnitIt &it, int4 s0, int4 s1) {
+__device__ __forceinline__ void it_start(UnitIt &it, int4 s0, int4 s1, const DecView &v) {
   it.i = s0.x;
   it.g = s0.y;
   it.kb = s0.z;
@@ -137,6 +143,8 @@ __device__ __forceinline__ void it_start(UnitIt &it, int4 s0, int4 s1) {
   it.units = s1.x;
   it.L = s1.y;
   it.uoff = s1.z;
+  it.seq = v.tok_seq ? v.tok_seq[it.tok] : 0;
+  it.pos = v.tok_pos ? v.tok_pos[it.tok] : 0;
 }
 
 __device__ __forceinline__ void it_next(UnitIt &it, const DecView &v) {
@@ -246,10 +254,13 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
   return *reinterpret_cast<uint32_t *>(&h);
 }
 
-template <int D, int G>
+// MASK: per-slot masked variant (the unified-span baseline): key j of a token is used
+// only if its slot holds a cell of the token's own sequence at a position up to the
+// token's own (cell_seq / cell_pos, copied into the stage with the block).
+template <int D, int G, bool MASK>
 __global__ void __launch_bounds__(kDecThreads, 1)
 k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
-  using Cfg = DecCfg<D, G>;
+  using Cfg = DecCfg<D, G, MASK>;
   constexpr int NS = Cfg::NS;
   constexpr int KSTEPS = D / 16;  // k-steps of the QK contraction
   constexpr int NT = D / 8;       // 8-dim tiles of the PV product
@@ -329,6 +340,8 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
   v.Hkv = a.Hkv;
   v.cap = a.max_pages * a.P;
   v.kv = a.kv;
+  v.tok_seq = MASK ? a.tok_seq : nullptr;
+  v.tok_pos = MASK ? a.tok_pos : nullptr;
   float *partials = reinterpret_cast<float *>(a.ws + a.lay.partials);
   int *dec_cnt = reinterpret_cast<int *>(a.ws + a.lay.dec_cnt);
 
@@ -358,7 +371,7 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
       const int pages_per_block = KB / a.P;
       const int oob_row = a.num_pages * a.Hkv * a.P;  // first row past the pool: zero fill
       UnitIt pit;
-      it_start(pit, start0, start1);
+      it_start(pit, start0, start1, v);
       int issued = 0;
       // page ids of the unit about to be issued, loaded one unit ahead (while the
       // producer waits for a free stage) so no global load sits on the issue path
@@ -405,9 +418,23 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
           m.units = pit.units;
           m.tok = pit.tok;
           m.seg_begin = a.Hkv * pit.uoff + pit.g * pit.units;
+          m.seq = pit.seq;
+          m.pos = pit.pos;
         }
         const uint32_t qbytes = seg_first ? (uint32_t)(G * D * 2) : 0u;
-        mbar_arrive_expect_tx(&bars->full[st], 2u * Cfg::kBlk + qbytes);
+        // masked variant: the (sequence, position) of each slot of the block's pages
+        const uint32_t cbytes = (MASK && rows > 0) ? (uint32_t)(2 * npg * a.P * 4) : 0u;
+        mbar_arrive_expect_tx(&bars->full[st], 2u * Cfg::kBlk + qbytes + cbytes);
+        if (MASK && rows > 0) {
+          unsigned char *cells = stage + 2 * Cfg::kBlk + Cfg::kQ;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (j >= npg) break;
+            const size_t slot0 = (size_t)pgs[j] * a.P;
+            bulk_g2s(cells + j * a.P * 4, a.cell_seq + slot0, a.P * 4, &bars->full[st]);
+            bulk_g2s(cells + KB * 4 + j * a.P * 4, a.cell_pos + slot0, a.P * 4, &bars->full[st]);
+          }
+        }
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           if (j >= pages_per_block) break;
@@ -650,7 +677,12 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int kk = t * 8 + 2 * cq + e;
-          x[t * 2 + e] = (kk < nr) ? s[t][e] * a.scale_log2 : -INFINITY;
+          bool ok = kk < nr;
+          if (MASK) {
+            const int *cs = reinterpret_cast<const int *>(stage + 2 * Cfg::kBlk + Cfg::kQ);
+            ok = ok && cs[key_base + kk] == cit.seq && cs[KB + key_base + kk] <= cit.pos;
+          }
+          x[t * 2 + e] = ok ? s[t][e] * a.scale_log2 : -INFINITY;
         }
       const float xm = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
       if (__any_sync(0xffffffffu, xm > m_run + kDecRescale)) {
@@ -680,6 +712,24 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
           for (int hf = 0; hf < Cfg::kHalves; ++hf)
             reinterpret_cast<uint4 *>(stage + Cfg::kBlk + hf * kBox + r * 128)[lane & 7] =
                 make_uint4(0, 0, 0, 0);
+        __syncwarp();
+        zeroed = true;
+      }
+      if (MASK) {
+        // so may the V rows of masked slots (free cells, other sequences' cells)
+        const int *cs = reinterpret_cast<const int *>(stage + 2 * Cfg::kBlk + Cfg::kQ);
+        const int kr = lane & 15;
+        const bool masked = kr < nr && !(cs[key_base + kr] == cit.seq &&
+                                         cs[KB + key_base + kr] <= cit.pos);
+        uint32_t bits = __ballot_sync(0xffffffffu, masked && lane < 16);
+        while (bits) {
+          const int r = key_base + __ffs(bits) - 1;
+          bits &= bits - 1;
+          // one row: Cfg::kHalves boxes x 8 chunks of 16 bytes
+          if (lane < Cfg::kHalves * 8)
+            reinterpret_cast<uint4 *>(stage + Cfg::kBlk + (lane >> 3) * kBox + r * 128)[lane & 7] =
+                make_uint4(0, 0, 0, 0);
+        }
         __syncwarp();
         zeroed = true;
       }
@@ -866,19 +916,19 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
   }
 }
 
-template <int D, int G>
+template <int D, int G, bool MASK>
 static cudaError_t launch_decode_t(const AttnArgs &a, int num_sms, const AttnMaps *maps,
                                    cudaStream_t s) {
-  using Cfg = DecCfg<D, G>;
+  using Cfg = DecCfg<D, G, MASK>;
   static bool attr_set = false;
   if (!attr_set) {
     // setmaxnreg.inc can only draw on registers the block was launched with: refuse to
     // launch (rather than wait forever) if the compiled allocation does not cover the split
     cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, k_decode<D, G>);
+    cudaError_t e = cudaFuncGetAttributes(&fa, k_decode<D, G, MASK>);
     if (e != cudaSuccess) return e;
     if (fa.numRegs * kDecThreads < kDecRegsSplitTotal) return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(k_decode<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(k_decode<D, G, MASK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Cfg::kSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
@@ -893,14 +943,17 @@ static cudaError_t launch_decode_t(const AttnArgs &a, int num_sms, const AttnMap
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_decode<D, G>, a, *maps);
+  return cudaLaunchKernelEx(&cfg, k_decode<D, G, MASK>, a, *maps);
 }
 
 cudaError_t launch_decode(const AttnArgs &a, int num_sms, const void *tmaps, cudaStream_t s) {
   const AttnMaps *maps = static_cast<const AttnMaps *>(tmaps);
   const int G = a.Hq / a.Hkv;
-#define PA_DEC_CASE(DD, GG) \
-  if (a.D == DD && G == GG) return launch_decode_t<DD, GG>(a, num_sms, maps, s);
+  const bool masked = a.cell_seq != nullptr;
+#define PA_DEC_CASE(DD, GG)                                                           \
+  if (a.D == DD && G == GG)                                                           \
+    return masked ? launch_decode_t<DD, GG, true>(a, num_sms, maps, s)                \
+                  : launch_decode_t<DD, GG, false>(a, num_sms, maps, s);
   PA_DEC_CASE(128, 1) PA_DEC_CASE(128, 2) PA_DEC_CASE(128, 4) PA_DEC_CASE(128, 8)
   PA_DEC_CASE(64, 1) PA_DEC_CASE(64, 2) PA_DEC_CASE(64, 4) PA_DEC_CASE(64, 8)
 #undef PA_DEC_CASE

@@ -31,6 +31,9 @@ struct AttnArgs {
   WsLayout lay;
   int max_pages, T, Hq, Hkv, P, D, num_pages;
   float scale_log2;  // scale * log2(e): softmax evaluated with exp2
+  // masked decode (unified-span baseline) only, else null: (sequence, position) of
+  // every slot of the pool and of every token
+  const int32_t *cell_seq, *cell_pos, *tok_seq, *tok_pos;
 };
 
 // Decode: split-KV over all SMs plus the log-sum-exp reduce.  Returns a

@@ -80,6 +80,31 @@ class Case:
         return spt
 
 
+def span_view(case: Case):
+    """The same cache seen as one span of cells shared by all sequences (the layout
+    paging replaces): every token's row names every page of the pool in order, its
+    kv_len is the whole span (0 for padding tokens), and each slot carries the
+    (sequence, position) of the cell it holds, -1 where free.  A page shared by two
+    sequences has no single owner per cell, so cases with shared pages are refused.
+    Returns (tok_page_table, tok_kv_len, cell_seq, cell_pos, tok_seq, tok_pos)."""
+    N, P = case.num_pages, case.P
+    cell_seq = np.full(N * P, -1, np.int32)
+    cell_pos = np.full(N * P, -1, np.int32)
+    for s, pages in enumerate(case.seq_pages):
+        L = int(case.seq_len[s])
+        pos = np.arange(L)
+        slots = np.asarray(pages, np.int64)[pos // P] * P + pos % P
+        if np.any(cell_seq[slots] != -1):
+            raise ValueError("span_view: a cell belongs to two sequences")
+        cell_seq[slots] = s
+        cell_pos[slots] = pos
+    T = case.T
+    tpt = np.tile(np.arange(N, dtype=np.int32), (T, 1))
+    kv = np.where(case.tok_seq >= 0, N * P, 0).astype(np.int32)
+    return (tpt, kv, cell_seq, cell_pos, case.tok_seq.astype(np.int32),
+            case.tok_pos.astype(np.int32))
+
+
 def _fill_pool(pool: np.ndarray, pages: np.ndarray, rows: np.ndarray, P: int, n_pos: int,
                skip_pos=None):
     """Lay rows [n_pos][Hkv][d] of one sequence into its pages (layout only)."""
