@@ -34,12 +34,14 @@ METRIC = "decode KV GB/s + prefill TFLOP/s, Qwen3-8B-shape paged attn, 8×16K, 1
 # digest of the kernel's sources at capture time: a kernel changed since then reports
 # traffic null.  k_prefill: mean of the 65 launches of one 8x16K step (launch list of
 # `bench.py --steps 2 --warmup 3 --no-cpu-baseline`); k_decode: one decode_8seq launch
-# (`profile_case decode`, cold L2); k_copy_pages: one launch of `profile_case copy`
+# (`profile_case decode`, cold L2); k_decode_span: one masked launch of
+# `profile_case span`; k_copy_pages: one launch of `profile_case copy`
 # (writes still in L2 at the end of the launch are not counted).  Summaries and
 # commands: profiles/.
 TRAFFIC = {
     "k_prefill": {"bytes": 676.1e6, "files": ["k_prefill.cu"], "digest": "d6b71aeae63528c1"},
-    "k_decode": {"bytes": 86.35e6, "files": ["k_decode.cu"], "digest": "255512206199014d"},
+    "k_decode": {"bytes": 86.01e6, "files": ["k_decode.cu"], "digest": "71e65c5d4c64acc7"},
+    "k_decode_span": {"bytes": 116.26e6, "files": ["k_decode.cu"], "digest": "71e65c5d4c64acc7"},
     "k_copy_pages": {"bytes": 488.0e6, "files": ["k_small.cu"], "digest": "aa9a77d695743686"},
 }
 _TRAFFIC_HEADERS = ["common.cuh", "tc.cuh", "tmap.cuh", "kernels.cuh"]
@@ -453,7 +455,10 @@ def bench_unified_span(pa, torch, db, steps, warmup, world, hbm, paged_ms_per_la
             "bytes_ratio": round(span_bytes / db.bytes_per_layer, 2),
             "roofline": {"bound": "hbm", "kernel": "k_decode (masked)", "achieved": round(gbs, 1),
                          "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4),
-                         "traffic": None},
+                         "traffic": traffic_of("k_decode_span"),
+                         "note": "achieved counts the span bytes each token must read; the 8 "
+                                 "tokens re-read one pool that fits in L2, so DRAM traffic is "
+                                 "about one pool per launch and L2 serves the rest"},
             "timing": "CUDA graph of 36 layers, each a plan + masked decode launch"}
 
 

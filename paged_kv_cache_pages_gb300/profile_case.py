@@ -9,6 +9,9 @@
       copies of the 82 MB pool used in turn (default 8: 660 MB, larger than L2,
       so every call streams its pool from HBM).
 
+  python -m paged_kv_cache_pages_gb300.profile_case span [--reps R]
+      the unified-span baseline on the decode layer: every token reads the whole
+      pool under a per-cell mask (one plan + masked decode per call).
   python -m paged_kv_cache_pages_gb300.profile_case copy [--reps R]
       page copy of copy-on-write forks: 512 of 1280 pages (8 KV heads x 128 rows
       x d 128, K and V) copied to 512 others per call.
@@ -100,6 +103,30 @@ def decode(reps: int, n_pools: int):
           f"({len(pools)} pools in turn, eager launches)")
 
 
+def span(reps: int):
+    c = workloads.decode(0)
+    dev = "cuda"
+    tpt0, kv0, slot = pa.expand_ubatch(
+        torch.from_numpy(c.seq_page_table()).to(dev), torch.from_numpy(c.tok_seq).to(dev),
+        torch.from_numpy(c.tok_pos).to(dev), c.P)
+    kp = torch.from_numpy(c.k_pool.view(np.float16)).to(dev)
+    vp = torch.from_numpy(c.v_pool.view(np.float16)).to(dev)
+    pa.kv_append(torch.from_numpy(c.k_new.view(np.float16)).to(dev),
+                 torch.from_numpy(c.v_new.view(np.float16)).to(dev), slot, kp, vp)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    tpt, kv, cs, cp, ts, tp = (t(a) for a in workloads.span_view(c))
+    q = torch.from_numpy(c.q.view(np.float16)).to(dev)
+    out = torch.empty_like(q)
+    ws = pa.new_workspace(c.T, c.Hq, c.Hkv, c.d, dev)
+    ms = _time(lambda: pa.masked_decode(q, kp, vp, tpt, kv, c.scale, cs, cp, ts, tp, out, ws),
+               reps)
+    if pa.read_error(ws):
+        raise SystemExit("device error word set")
+    nbytes = float(c.T) * c.num_pages * c.Hkv * c.P * c.d * 4
+    print(f"span: {ms * 1e3:.1f} us/call {nbytes / ms / 1e6:.1f} GB/s of span reads "
+          f"({c.num_pages} pages read by each of {c.T} tokens)")
+
+
 def copy(reps: int):
     dev = "cuda"
     N, Hkv, P, d, n = 1280, 8, 128, 128, 512
@@ -116,7 +143,7 @@ def copy(reps: int):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["prefill", "decode", "copy"])
+    ap.add_argument("case", choices=["prefill", "decode", "copy", "span"])
     ap.add_argument("--ubatch", type=int, default=48)
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--pools", type=int, default=8)
@@ -125,6 +152,8 @@ def main():
         prefill(a.ubatch, a.reps)
     elif a.case == "decode":
         decode(a.reps, a.pools)
+    elif a.case == "span":
+        span(a.reps)
     else:
         copy(a.reps)
 
