@@ -437,6 +437,7 @@ def bench_unified_span(pa, torch, db, steps, warmup, world, hbm, paged_ms_per_la
     out = torch.empty_like(db.q[0])
 
     def step():
+        pa.plan_decode(tpt, kv, c.Hq, c.Hkv, c.P, c.d, ws)
         for l in range(db.layers):
             kp, vp = db.pools[l]
             pa.masked_decode(db.q[l], kp, vp, tpt, kv, c.scale, cs, cp, ts, tp, out, ws)
@@ -459,7 +460,51 @@ def bench_unified_span(pa, torch, db, steps, warmup, world, hbm, paged_ms_per_la
                          "note": "achieved counts the span bytes each token must read; the 8 "
                                  "tokens re-read one pool that fits in L2, so DRAM traffic is "
                                  "about one pool per launch and L2 serves the rest"},
-            "timing": "CUDA graph of 36 layers, each a plan + masked decode launch"}
+            "timing": "CUDA graph of one plan and 36 masked decode launches (one per layer)"}
+
+
+def bench_fp8_decode(pa, torch, db, steps, warmup, world, hbm, f16_ms_per_layer):
+    """FP8 KV pages on the decode workload: the same 36 layers with every cached row
+    quantised (E4M3 codes, one scale per row) by the library's quantising append;
+    one plan, then 36 FP8 decode launches back to back."""
+    c = db.case
+    dev = db.q[0].device
+    rows_k, rows_v, slots = [], [], []
+    for s_, pages in enumerate(c.seq_pages):
+        L = int(c.seq_len[s_])
+        pos = np.arange(L)
+        slots.append(np.asarray(pages, np.int64)[pos // c.P] * c.P + pos % c.P)
+        rows_k.append(c.k_ctx[s_][:L])
+        rows_v.append(c.v_ctx[s_][:L])
+    kr = torch.from_numpy(np.concatenate(rows_k).view(np.float16)).to(dev)
+    vr = torch.from_numpy(np.concatenate(rows_v).view(np.float16)).to(dev)
+    sl = torch.from_numpy(np.concatenate(slots)).to(dev)
+    base = pa.new_fp8_pool(c.num_pages, c.Hkv, c.P, c.d, dev)
+    pa.kv_append_fp8(kr, vr, sl, *base)
+    pools = [base] + [tuple(t.clone() for t in base) for _ in range(db.layers - 1)]
+    ws = pa.new_workspace(c.T, c.Hq, c.Hkv, c.d, dev)
+    out = torch.empty_like(db.q[0])
+
+    def step():
+        pa.plan_decode(db.tpt, db.kv, c.Hq, c.Hkv, c.P, c.d, ws)
+        for l in range(db.layers):
+            pa.decode_fp8(db.q[l], *pools[l], db.tpt, db.kv, c.scale, out, ws)
+
+    g = capture_step(torch, step)
+    total_ms, _ = time_steps(torch, g.replay, steps, warmup, world)
+    ms_layer = max_over_ranks(total_ms / steps / db.layers, world)
+    if pa.read_error(ws):
+        raise RuntimeError("device error word set in the FP8 decode")
+    nbytes = float(c.seq_len.astype(np.int64).sum()) * c.Hkv * (2 * c.d + 2 * 4)
+    gbs = nbytes / (ms_layer / 1e3) / 1e9
+    return {"workload": "decode_8seq_fp8_pages", "unit": "GB/s", "value": round(gbs * world, 1),
+            "ms_per_layer": round(ms_layer, 4), "bytes_per_layer": nbytes,
+            "f16_ms_per_layer": round(f16_ms_per_layer, 4),
+            "speedup_vs_f16": round(f16_ms_per_layer / ms_layer, 2),
+            "roofline": {"bound": "hbm", "kernel": "k_decode (FP8 pages)",
+                         "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                         "frac": round(gbs / hbm, 4), "traffic": None},
+            "timing": "CUDA graph of one plan and 36 FP8 decode launches (one per layer)"}
 
 
 def run_ours(args):
@@ -566,6 +611,8 @@ def run_ours(args):
             with_cpu=rank == 0 and world == 1 and not args.no_cpu_baseline, seed=args.seed),
         "unified_span": bench_unified_span(pa, torch, db, args.steps, args.warmup, world, hbm,
                                            d_kt * 1e3),
+        "fp8_pages": bench_fp8_decode(pa, torch, db, args.steps, args.warmup, world, hbm,
+                                      d_kt * 1e3),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_prefill(pb.wl, budget_s=args.cpu_budget)

@@ -200,6 +200,15 @@ int paged_attn_validate(const int32_t *tok_page_table, int max_pages, const int3
                         int T, int P, int num_pages, int *err, void *stream);
 
 /*
+ * paged_attn_plan with every token routed to the split-KV path (none to the
+ * tensor-core tiles): the plan that paged_attn_masked_decode and
+ * paged_attn_decode_fp8 run on.  Arguments as paged_attn_plan.
+ */
+int paged_attn_plan_decode(const int32_t *tok_page_table, int max_pages,
+                           const int32_t *tok_kv_len, int T, int Hq, int Hkv, int P, int d,
+                           void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Unified-span baseline (UA-PagedAttention page, section 作品简介: the original
  * llama.cpp cache is one span of cells shared by all sequences, and attention
  * reads the whole span under a mask that keeps each query's own sequence).
@@ -213,9 +222,10 @@ int paged_attn_validate(const int32_t *tok_page_table, int max_pages, const int3
  *   cell_seq, cell_pos [num_pages * P] int32 (device, 16-byte aligned): the
  *       sequence (-1 = free) and position of the cell in each slot
  *   tok_seq, tok_pos [T] int32 (device): each token's sequence and position
- *   other arguments as paged_attn_forward.  Plans on its own (every token goes
- *   to the split-KV path) and writes out for every token.  A token whose mask
- *   keeps no key gets a zero row.
+ *   other arguments as paged_attn_forward.  Runs on the workspace's plan, which
+ *   must come from paged_attn_plan_decode (every token on the split-KV path) for
+ *   the same tables; writes out for every token.  A token whose mask keeps no
+ *   key gets a zero row.
  */
 int paged_attn_masked_decode(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
                              const int32_t *tok_page_table, int max_pages,
@@ -224,6 +234,41 @@ int paged_attn_masked_decode(const uint16_t *q, const uint16_t *k_pages, const u
                              const int32_t *cell_pos, const int32_t *tok_seq,
                              const int32_t *tok_pos, uint16_t *out, void *workspace,
                              size_t workspace_bytes, void *stream);
+
+/*
+ * Reduced-precision KV pages: FP8 E4M3 codes with one binary32 scale per cached
+ * row (token, KV head) -- the adaptive KV quantisation the
+ * "面向边缘智能体推理的 llama.cpp KV Cache 共享与复用优化" page names; on the
+ * UA-PagedAttention page the KV cache is binary16.  Decode streams half the bytes.
+ *
+ * Quantising reshape-and-cache: for each token with slot >= 0 and each KV head,
+ * scale = amax(row) / 448 in binary32 (1 for an all-zero row) and
+ * code_i = E4M3(x_i / scale) (nearest, ties to even, saturating at +-448).
+ *   k, v [T][Hkv][d] binary16; slot_mapping [T] int64 (as paged_kv_append)
+ *   k8_pages  [num_pages][Hkv][P][d] uint8   K codes, one row per cached token
+ *   v8t_pages [num_pages][Hkv][d][P] uint8   V codes, transposed in each block
+ *   k_scale, v_scale [num_pages][Hkv][P] float
+ *   err (device, optional): PA_ERR_SLOT_RANGE for a slot beyond the pool.
+ * d must be a multiple of 32, at most 128.  Bit-exact against the reference
+ * quantiser.  One launch.
+ */
+int paged_kv_append_fp8(const uint16_t *k, const uint16_t *v, const int64_t *slot_mapping, int T,
+                        uint8_t *k8_pages, uint8_t *v8t_pages, float *k_scale, float *v_scale,
+                        int num_pages, int Hkv, int P, int d, int *err, void *stream);
+
+/*
+ * Split-KV decode attention over FP8 pages (layout above; page size 128, d 128,
+ * scale arrays 16-byte aligned): K_t[j] = E4M3(k8) * k_scale, V_t[j] likewise.
+ * Runs on the workspace's plan, which must come from paged_attn_plan_decode for
+ * the same tables (one plan serves every layer); writes out for every token;
+ * other arguments as paged_attn_forward.  PA_EUNSUPPORTED for another page size
+ * or head dimension.
+ */
+int paged_attn_decode_fp8(const uint16_t *q, const uint8_t *k8_pages, const uint8_t *v8t_pages,
+                          const float *k_scale, const float *v_scale,
+                          const int32_t *tok_page_table, int max_pages, const int32_t *tok_kv_len,
+                          int T, int Hq, int Hkv, int P, int d, int num_pages, float scale,
+                          uint16_t *out, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Page copy for copy-on-write forks (CacheFlow page, section 核心架构 2: blocks

@@ -70,6 +70,19 @@ def _load():
                                                  c_double, i32p, i32p, i32p, i32p,
                                                  ctypes.c_void_p, c_int, f64p]
             lib.ref_masked_attention.restype = c_int
+            u8p = np.ctypeslib.ndpointer(np.uint8, flags="C_CONTIGUOUS")
+            f32p = np.ctypeslib.ndpointer(np.float32, flags="C_CONTIGUOUS")
+            lib.ref_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+            lib.ref_e4m3_to_f64.restype = c_double
+            lib.ref_f32_to_e4m3.argtypes = [ctypes.c_float]
+            lib.ref_f32_to_e4m3.restype = ctypes.c_uint8
+            lib.ref_kv_append_fp8.argtypes = [u16p, u16p, i64p, c_int, u8p, u8p, f32p, f32p,
+                                              c_int, c_int, c_int, c_int]
+            lib.ref_kv_append_fp8.restype = c_int
+            lib.ref_paged_attention_fp8.argtypes = [u16p, u8p, u8p, f32p, f32p, i32p, c_int, i32p,
+                                                    c_int, c_int, c_int, c_int, c_int, c_int,
+                                                    c_double, ctypes.c_void_p, c_int, f64p]
+            lib.ref_paged_attention_fp8.restype = c_int
             lib.ref_num_threads.argtypes = []
             lib.ref_num_threads.restype = c_int
             _lib = lib
@@ -193,4 +206,56 @@ def masked_attention(q, k_pages, v_pages, tok_page_table, tok_kv_len, scale, cel
                                       N, float(scale), cs, cp, ts, tp, sel, n, out)
     if rc != 0:
         raise ValueError("masked_attention: page id or kv_len out of range")
+    return out
+
+
+def e4m3_to_f64(code: int) -> float:
+    """Value of one FP8 E4M3 code."""
+    return float(_load().ref_e4m3_to_f64(int(code)))
+
+
+def f32_to_e4m3(x: float) -> int:
+    """E4M3 code of a binary32 value: nearest, ties to even, saturating at 448."""
+    return int(_load().ref_f32_to_e4m3(float(np.float32(x))))
+
+
+def kv_append_fp8(k, v, slot_mapping, k8, v8t, k_scale, v_scale):
+    """Quantising reshape-and-cache on host arrays (updated in place):
+    k8 [N][Hkv][P][d] uint8, v8t [N][Hkv][d][P] uint8, scales [N][Hkv][P] float32."""
+    k = _c(k, np.uint16)
+    v = _c(v, np.uint16)
+    slot = _c(slot_mapping, np.int64)
+    for a, dt in ((k8, np.uint8), (v8t, np.uint8), (k_scale, np.float32), (v_scale, np.float32)):
+        assert a.flags.c_contiguous and a.dtype == dt
+    N, Hkv, P, d = k8.shape
+    rc = _load().ref_kv_append_fp8(k, v, slot, slot.shape[0], k8, v8t, k_scale, v_scale, N, Hkv,
+                                   P, d)
+    if rc != 0:
+        raise ValueError("kv_append_fp8: slot beyond the pool")
+
+
+def paged_attention_fp8(q, k8, v8t, k_scale, v_scale, tok_page_table, tok_kv_len, scale,
+                        tokens=None):
+    """fp64 paged attention over FP8 pages (dequantised by definition)."""
+    q = _c(q, np.uint16)
+    k8, v8t = _c(k8, np.uint8), _c(v8t, np.uint8)
+    ks, vs = _c(k_scale, np.float32), _c(v_scale, np.float32)
+    tpt = _c(tok_page_table, np.int32)
+    kv = _c(tok_kv_len, np.int32)
+    T, Hq, d = q.shape
+    N, Hkv, P, d2 = k8.shape
+    assert d2 == d and Hq % Hkv == 0
+    if tokens is None:
+        sel, n = None, T
+    else:
+        tok_arr = _c(tokens, np.int32)
+        n = tok_arr.shape[0]
+        sel = tok_arr.ctypes.data_as(ctypes.c_void_p)
+    out = np.zeros((n, Hq, d), np.float64)
+    if n == 0:
+        return out
+    rc = _load().ref_paged_attention_fp8(q, k8, v8t, ks, vs, tpt, tpt.shape[1], kv, T, Hq, Hkv, P,
+                                         d, N, float(scale), sel, n, out)
+    if rc != 0:
+        raise ValueError("paged_attention_fp8: page id or kv_len out of range")
     return out

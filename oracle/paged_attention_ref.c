@@ -280,6 +280,162 @@ int ref_masked_attention(const uint16_t *q, const uint16_t *k_pages, const uint1
     return bad ? -1 : 0;
 }
 
+/*
+ * Reduced-precision KV pages (the adaptive KV quantisation named on the
+ * "面向边缘智能体推理的 llama.cpp KV Cache 共享与复用优化" page; the model's KV
+ * stays binary16 on the UA-PagedAttention page): FP8 E4M3 codes with one scale
+ * per cached row (token, KV head).
+ *
+ * E4M3 ("fn" variant of the OCP 8-bit floating point formats): 1 sign bit, 4
+ * exponent bits with bias 7, 3 mantissa bits; exponent 0 encodes subnormals
+ * m/8 * 2^-6; the all-ones pattern (S.1111.111) is NaN; there is no infinity;
+ * the largest finite magnitude is 1.75 * 2^8 = 448.
+ */
+double ref_e4m3_to_f64(uint8_t c)
+{
+    int sign = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m / 8.0, -6);
+    else v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/*
+ * Round x to the nearest E4M3 value, ties to the code with an even mantissa,
+ * magnitudes past 448 to +-448 (saturating), NaN to NaN: a search over the 127
+ * finite non-negative codes.
+ */
+uint8_t ref_f32_to_e4m3(float x)
+{
+    if (x != x) return 0x7F;
+    uint8_t sign = signbit(x) ? 0x80 : 0;
+    double a = fabs((double)x);
+    if (a >= 448.0) return sign | 0x7E;
+    int best = 0;
+    double best_err = a;  /* distance to code 0 */
+    for (int c = 1; c <= 0x7E; ++c) {
+        double err = fabs(ref_e4m3_to_f64((uint8_t)c) - a);
+        if (err < best_err || (err == best_err && (c & 1) == 0 && (best & 1) == 1)) {
+            best = c;
+            best_err = err;
+        }
+    }
+    return sign | (uint8_t)best;
+}
+
+/*
+ * Quantise one binary16 row of n values: scale = amax / 448 in binary32 (1 if
+ * the row is all zeros), code_i = E4M3(x_i / scale) with the division in binary32.
+ */
+static float quantise_row(const uint16_t *x, int n, uint8_t *codes, size_t stride)
+{
+    float amax = 0.f;
+    for (int i = 0; i < n; ++i) {
+        float v = fabsf((float)ref_f16_to_f64(x[i]));
+        if (v > amax) amax = v;
+    }
+    float scale = amax > 0.f ? amax / 448.0f : 1.0f;
+    for (int i = 0; i < n; ++i)
+        codes[(size_t)i * stride] = ref_f32_to_e4m3((float)ref_f16_to_f64(x[i]) / scale);
+    return scale;
+}
+
+/*
+ * Quantising reshape-and-cache into FP8 pages.  For each token with slot >= 0
+ * and each KV head h, the row of k (and of v) is quantised (quantise_row) and
+ * written at page = slot / P, offset = slot % P:
+ *   k8  [num_pages][Hkv][P][d]  codes, one row per cached token (as the f16 pool)
+ *   v8t [num_pages][Hkv][d][P]  codes, transposed inside each (page, head) block
+ *   k_scale, v_scale [num_pages][Hkv][P]  binary32 scale of each row
+ * Returns 0, or -1 if a slot is beyond the pool.
+ */
+int ref_kv_append_fp8(const uint16_t *k, const uint16_t *v, const int64_t *slot_mapping, int T,
+                      uint8_t *k8, uint8_t *v8t, float *k_scale, float *v_scale, int num_pages,
+                      int Hkv, int P, int d)
+{
+    for (int t = 0; t < T; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;
+        if (slot >= (int64_t)num_pages * P) return -1;
+        int64_t page = slot / P, off = slot % P;
+        for (int h = 0; h < Hkv; ++h) {
+            size_t row = ((size_t)page * Hkv + h) * P + off;
+            const uint16_t *kr = k + ((size_t)t * Hkv + h) * d;
+            const uint16_t *vr = v + ((size_t)t * Hkv + h) * d;
+            k_scale[row] = quantise_row(kr, d, k8 + row * d, 1);
+            v_scale[row] = quantise_row(vr, d, v8t + ((size_t)page * Hkv + h) * d * P + off, P);
+        }
+    }
+    return 0;
+}
+
+/*
+ * Paged attention over FP8 pages: as ref_paged_attention, with
+ *   K_t[j][i] = e4m3(k8[page][g][j % P][i]) * k_scale[page][g][j % P]
+ *   V_t[j][i] = e4m3(v8t[page][g][i][j % P]) * v_scale[page][g][j % P]
+ * (page = tok_page_table[t][j / P]), all in double.
+ */
+int ref_paged_attention_fp8(const uint16_t *q, const uint8_t *k8, const uint8_t *v8t,
+                            const float *k_scale, const float *v_scale,
+                            const int32_t *tok_page_table, int max_pages,
+                            const int32_t *tok_kv_len, int T, int Hq, int Hkv, int P, int d,
+                            int num_pages, double scale, const int32_t *tokens, int n_tok,
+                            double *out)
+{
+    int G = Hq / Hkv;
+    int n = tokens ? n_tok : T;
+    int bad = 0;
+    long long pairs = (long long)n * Hq;
+#pragma omp parallel for schedule(dynamic, 1) reduction(|: bad)
+    for (long long pi = 0; pi < pairs; ++pi) {
+        int ti = (int)(pi / Hq), h = (int)(pi % Hq);
+        int t = tokens ? tokens[ti] : ti;
+        int g = h / G;
+        int L = tok_kv_len[t];
+        double *o = out + ((size_t)ti * Hq + h) * d;
+        for (int i = 0; i < d; ++i) o[i] = 0.0;
+        if (L <= 0) continue;
+        if (L > max_pages * P) { bad = 1; continue; }
+        double *Kt = (double *)malloc(sizeof(double) * (size_t)L * d);
+        double *Vt = (double *)malloc(sizeof(double) * (size_t)L * d);
+        double *s = (double *)malloc(sizeof(double) * (size_t)L);
+        const int32_t *row = tok_page_table + (size_t)t * max_pages;
+        int ok = 1;
+        /* gather and dequantise this token's keys and values */
+        for (int j = 0; j < L && ok; ++j) {
+            int page = row[j / P];
+            if (page < 0 || page >= num_pages) { ok = 0; break; }
+            size_t r = ((size_t)page * Hkv + g) * P + (j % P);
+            size_t vb = ((size_t)page * Hkv + g) * d * P + (j % P);
+            for (int i = 0; i < d; ++i) {
+                Kt[(size_t)j * d + i] = ref_e4m3_to_f64(k8[r * d + i]) * (double)k_scale[r];
+                Vt[(size_t)j * d + i] = ref_e4m3_to_f64(v8t[vb + (size_t)i * P]) * (double)v_scale[r];
+            }
+        }
+        if (ok) {
+            const uint16_t *qh = q + ((size_t)t * Hq + h) * d;
+            double m = -INFINITY;
+            for (int j = 0; j < L; ++j) {
+                double acc = 0.0;
+                for (int i = 0; i < d; ++i) acc += ref_f16_to_f64(qh[i]) * Kt[(size_t)j * d + i];
+                s[j] = scale * acc;
+                if (s[j] > m) m = s[j];
+            }
+            double Z = 0.0;
+            for (int j = 0; j < L; ++j) { s[j] = exp(s[j] - m); Z += s[j]; }
+            for (int j = 0; j < L; ++j) {
+                double w = s[j] / Z;
+                for (int i = 0; i < d; ++i) o[i] += w * Vt[(size_t)j * d + i];
+            }
+        } else {
+            bad = 1;
+        }
+        free(Kt); free(Vt); free(s);
+    }
+    return bad ? -1 : 0;
+}
+
 /* Number of threads the OpenMP runtime will use (reported beside CPU timings). */
 int ref_num_threads(void)
 {

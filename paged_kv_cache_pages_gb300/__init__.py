@@ -12,6 +12,7 @@ Entry points mirror include/paged_attn.h:
   kv_append       reshape-and-cache into the paged pool
   copy_pages      page copy of a copy-on-write fork
   masked_decode   the unified-span baseline (masked attention over a shared span)
+  kv_append_fp8 / decode_fp8   FP8 (E4M3) KV pages with per-row scales
   plan / prefill / decode / run / forward   the attention itself
   validate, read_error, set_prefill_min_run, workspace_size
   PagePool        host page allocator with reference-counted sharing
@@ -63,6 +64,11 @@ _SIGS = {
     "pa_pool_refcount": ([_vp, ctypes.c_int32], _i),
     "pa_pool_fork": ([_vp, _vp, _i, _i, _vp, _vp, _vp], _i),
     "paged_copy_pages": ([_vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _vp, _vp], _i),
+    "paged_kv_append_fp8": ([_vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp],
+                            _i),
+    "paged_attn_decode_fp8": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i,
+                               ctypes.c_float, _vp, _vp, _sz, _vp], _i),
+    "paged_attn_plan_decode": ([_vp, _i, _vp, _i, _i, _i, _i, _i, _vp, _sz, _vp], _i),
     "paged_attn_masked_decode": ([_vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i,
                                   ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i),
 }
@@ -152,11 +158,21 @@ def kv_append(k, v, slot_mapping, k_pages, v_pages, err=None, stream=None):
            "paged_kv_append")
 
 
+def plan_decode(tok_page_table, tok_kv_len, Hq, Hkv, P, d, workspace, stream=None):
+    """plan with every token on the split-KV path (for masked_decode / decode_fp8)."""
+    _req(tok_page_table, torch.int32, "tok_page_table")
+    _req(tok_kv_len, torch.int32, "tok_kv_len")
+    T, max_pages = tok_page_table.shape
+    _check(_lib.paged_attn_plan_decode(_ptr(tok_page_table), max_pages, _ptr(tok_kv_len), T, Hq,
+                                       Hkv, P, d, _ptr(workspace), workspace.numel(),
+                                       _stream(stream)), "paged_attn_plan_decode")
+
+
 def masked_decode(q, k_pages, v_pages, tok_page_table, tok_kv_len, scale, cell_seq, cell_pos,
                   tok_seq, tok_pos, out, workspace, stream=None):
     """Unified-span baseline: split-KV attention of every token over its row, keeping
     only the slots whose cell belongs to the token's sequence at a position up to its
-    own.  Plans on its own."""
+    own.  Runs on a plan from plan_decode."""
     for t, n in ((q, "q"), (k_pages, "k_pages"), (v_pages, "v_pages"), (out, "out")):
         _req(t, torch.float16, n)
     for t, n in ((tok_page_table, "tok_page_table"), (tok_kv_len, "tok_kv_len"),
@@ -171,6 +187,47 @@ def masked_decode(q, k_pages, v_pages, tok_page_table, tok_kv_len, scale, cell_s
         T, Hq, Hkv, P, d, N, float(scale), _ptr(cell_seq), _ptr(cell_pos), _ptr(tok_seq),
         _ptr(tok_pos), _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)),
         "paged_attn_masked_decode")
+    return out
+
+
+def new_fp8_pool(num_pages, Hkv, P, d, device=None):
+    """Empty FP8 pool: (k8 [N][Hkv][P][d] uint8, v8t [N][Hkv][d][P] uint8,
+    k_scale, v_scale [N][Hkv][P] float32)."""
+    dev = device or "cuda"
+    return (torch.zeros((num_pages, Hkv, P, d), dtype=torch.uint8, device=dev),
+            torch.zeros((num_pages, Hkv, d, P), dtype=torch.uint8, device=dev),
+            torch.ones((num_pages, Hkv, P), dtype=torch.float32, device=dev),
+            torch.ones((num_pages, Hkv, P), dtype=torch.float32, device=dev))
+
+
+def kv_append_fp8(k, v, slot_mapping, k8, v8t, k_scale, v_scale, err=None, stream=None):
+    """Quantising reshape-and-cache into FP8 pages (E4M3 codes, one scale per row)."""
+    _req(k, torch.float16, "k")
+    _req(v, torch.float16, "v")
+    _req(slot_mapping, torch.int64, "slot_mapping")
+    for t, n in ((k8, "k8"), (v8t, "v8t")):
+        _req(t, torch.uint8, n)
+    for t, n in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+        _req(t, torch.float32, n)
+    N, Hkv, P, d = k8.shape
+    _check(_lib.paged_kv_append_fp8(_ptr(k), _ptr(v), _ptr(slot_mapping), slot_mapping.shape[0],
+                                    _ptr(k8), _ptr(v8t), _ptr(k_scale), _ptr(v_scale), N, Hkv, P,
+                                    d, _ptr(err), _stream(stream)), "paged_kv_append_fp8")
+
+
+def decode_fp8(q, k8, v8t, k_scale, v_scale, tok_page_table, tok_kv_len, scale, out, workspace,
+               stream=None):
+    """Split-KV decode attention over FP8 pages (runs on a plan from plan_decode)."""
+    _req(q, torch.float16, "q")
+    _req(out, torch.float16, "out")
+    _req(tok_page_table, torch.int32, "tok_page_table")
+    _req(tok_kv_len, torch.int32, "tok_kv_len")
+    T, Hq, d = q.shape
+    N, Hkv, P, _ = k8.shape
+    _check(_lib.paged_attn_decode_fp8(
+        _ptr(q), _ptr(k8), _ptr(v8t), _ptr(k_scale), _ptr(v_scale), _ptr(tok_page_table),
+        tok_page_table.shape[1], _ptr(tok_kv_len), T, Hq, Hkv, P, d, N, float(scale), _ptr(out),
+        _ptr(workspace), workspace.numel(), _stream(stream)), "paged_attn_decode_fp8")
     return out
 
 

@@ -87,6 +87,7 @@ AttnArgs make_args(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v
   a.num_pages = num_pages;
   a.scale_log2 = scale * kLog2e;
   a.cell_seq = a.cell_pos = a.tok_seq = a.tok_pos = nullptr;
+  a.k_scale = a.v_scale = nullptr;
   return a;
 }
 
@@ -148,6 +149,49 @@ int paged_kv_append(const uint16_t *k, const uint16_t *v, const int64_t *slot_ma
   return launch_status(cudaGetLastError());
 }
 
+static int plan_with(const int32_t *tok_page_table, int max_pages, const int32_t *tok_kv_len,
+                     int T, int Hq, int Hkv, int P, int d, void *workspace,
+                     size_t workspace_bytes, void *stream, int min_run);
+
+int paged_kv_append_fp8(const uint16_t *k, const uint16_t *v, const int64_t *slot_mapping, int T,
+                        uint8_t *k8_pages, uint8_t *v8t_pages, float *k_scale, float *v_scale,
+                        int num_pages, int Hkv, int P, int d, int *err, void *stream) {
+  if (T < 0 || num_pages < 0 || Hkv <= 0 || P <= 0 || d <= 0) return PA_EINVAL;
+  if (d > 128 || d % 32 != 0) return PA_EUNSUPPORTED;
+  if (T == 0) return PA_OK;
+  if (!k || !v || !slot_mapping || !k8_pages || !v8t_pages || !k_scale || !v_scale)
+    return PA_EINVAL;
+  const long long rows = (long long)T * Hkv;
+  int blocks = (int)std::min<long long>((rows + 7) / 8, (long long)sm_count() * 16);
+  if (blocks < 1) blocks = 1;
+  k_append_fp8<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      k, v, slot_mapping, T, k8_pages, v8t_pages, k_scale, v_scale, num_pages, Hkv, P, d, err);
+  return launch_status(cudaGetLastError());
+}
+
+int paged_attn_decode_fp8(const uint16_t *q, const uint8_t *k8_pages, const uint8_t *v8t_pages,
+                          const float *k_scale, const float *v_scale,
+                          const int32_t *tok_page_table, int max_pages, const int32_t *tok_kv_len,
+                          int T, int Hq, int Hkv, int P, int d, int num_pages, float scale,
+                          uint16_t *out, void *workspace, size_t workspace_bytes, void *stream) {
+  const uint16_t *kp = reinterpret_cast<const uint16_t *>(k8_pages);
+  const uint16_t *vp = reinterpret_cast<const uint16_t *>(v8t_pages);
+  int st = check_attn(q, kp, vp, tok_page_table, max_pages, tok_kv_len, T, Hq, Hkv, P, d,
+                      num_pages, out, workspace, workspace_bytes, true);
+  if (st != PA_OK || T == 0) return st;
+  if (P != 128 || d != 128) return PA_EUNSUPPORTED;
+  if (!k_scale || !v_scale) return PA_EINVAL;
+  if (!aligned16(k_scale) || !aligned16(v_scale)) return PA_EALIGN;
+  AttnArgs a = make_args(q, kp, vp, tok_page_table, max_pages, tok_kv_len, T, Hq, Hkv, P, d,
+                         num_pages, scale, out, workspace);
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  AttnMaps maps;
+  st = encode_attn_maps_fp8(a, &maps);
+  if (st != PA_OK) return st;
+  return launch_status(launch_decode(a, sm_count(), &maps, static_cast<cudaStream_t>(stream)));
+}
+
 int paged_copy_pages(const int32_t *src, const int32_t *dst, int n, uint16_t *k_pages,
                      uint16_t *v_pages, int num_pages, int Hkv, int P, int d, int *err,
                      void *stream) {
@@ -202,6 +246,13 @@ int paged_attn_plan(const int32_t *tok_page_table, int max_pages, const int32_t 
                    workspace_bytes, stream, g_min_run.load());
 }
 
+int paged_attn_plan_decode(const int32_t *tok_page_table, int max_pages,
+                           const int32_t *tok_kv_len, int T, int Hq, int Hkv, int P, int d,
+                           void *workspace, size_t workspace_bytes, void *stream) {
+  return plan_with(tok_page_table, max_pages, tok_kv_len, T, Hq, Hkv, P, d, workspace,
+                   workspace_bytes, stream, INT_MAX);
+}
+
 int paged_attn_masked_decode(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
                              const int32_t *tok_page_table, int max_pages,
                              const int32_t *tok_kv_len, int T, int Hq, int Hkv, int P, int d,
@@ -214,10 +265,6 @@ int paged_attn_masked_decode(const uint16_t *q, const uint16_t *k_pages, const u
   if (st != PA_OK || T == 0) return st;
   if (!cell_seq || !cell_pos || !tok_seq || !tok_pos) return PA_EINVAL;
   if (!aligned16(cell_seq) || !aligned16(cell_pos)) return PA_EALIGN;
-  // every token on the split-KV path (the tensor-core tiles have no per-key mask)
-  st = plan_with(tok_page_table, max_pages, tok_kv_len, T, Hq, Hkv, P, d, workspace,
-                 workspace_bytes, stream, INT_MAX);
-  if (st != PA_OK) return st;
   AttnArgs a = make_args(q, k_pages, v_pages, tok_page_table, max_pages, tok_kv_len, T, Hq, Hkv, P,
                          d, num_pages, scale, out, workspace);
   a.cell_seq = cell_seq;

@@ -44,13 +44,16 @@ static_assert(kKeysPerWarp == 16, "warp key slice is 16 rows");
 
 constexpr int kBarBytes = 1024;  // barriers, stage metadata, jobs, flags
 
-template <int D, int G, bool MASK>
+template <int D, int G, bool MASK, bool KV8>
 struct DecCfg {
-  static constexpr int kHalves = D / 64;
-  static constexpr int kBlk = kHalves * kBox;                 // one block of K (or V)
+  static_assert(!(MASK && KV8), "one variant at a time");
+  static_assert(!KV8 || D == 128, "FP8 pages: 128-byte rows");
+  static constexpr int kHalves = KV8 ? 1 : D / 64;
+  static constexpr int kBlk = KV8 ? KB * D : kHalves * kBox;  // one block of K (or V)
   static constexpr int kQ = ((G * D * 2) + 1023) / 1024 * 1024;  // the group's query rows
   static constexpr int kCells = MASK ? 2 * KB * 4 : 0;        // (sequence, position) of each key
-  static constexpr int kStage = 2 * kBlk + kQ + kCells;       // multiple of 1024
+  static constexpr int kScales = KV8 ? 2 * KB * 4 : 0;        // K and V scale of each key
+  static constexpr int kStage = 2 * kBlk + kQ + kCells + kScales;  // multiple of 1024
   static constexpr int kMergeDims = 64;                       // the warps merge 64 dims at a time
   static constexpr int kMerge = kDecWarps * G * (kMergeDims + 2) * 4;
   static constexpr int kPart = G * (D + 2) * 4;               // one split partial (m, l, acc)
@@ -249,6 +252,17 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
 __device__ __forceinline__ uint32_t sw128(int r, int c) {
   return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
 }
+// Two FP8 E4M3 codes (the low byte is the element of the lower index) widened to f16x2
+// (exact: every E4M3 value is a binary16 value).
+__device__ __forceinline__ uint32_t e4m3x2_to_h2(uint16_t c) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(c));
+  return r;
+}
+__device__ __forceinline__ uint16_t lds_u16(const unsigned char *p) {
+  return *reinterpret_cast<const uint16_t *>(p);
+}
+
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&h);
@@ -257,10 +271,14 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
 // MASK: per-slot masked variant (the unified-span baseline): key j of a token is used
 // only if its slot holds a cell of the token's own sequence at a position up to the
 // token's own (cell_seq / cell_pos, copied into the stage with the block).
-template <int D, int G, bool MASK>
+// KV8: FP8 pages (E4M3 codes, one scale per cached row; V transposed inside each
+// (page, head) block; page size 128, d 128): the consumers widen the codes to f16
+// for the same tensor-path contractions, apply the K scales to the scores and fold
+// the V scales into P.
+template <int D, int G, bool MASK, bool KV8>
 __global__ void __launch_bounds__(kDecThreads, 1)
 k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
-  using Cfg = DecCfg<D, G, MASK>;
+  using Cfg = DecCfg<D, G, MASK, KV8>;
   constexpr int NS = Cfg::NS;
   constexpr int KSTEPS = D / 16;  // k-steps of the QK contraction
   constexpr int NT = D / 8;       // 8-dim tiles of the PV product
@@ -319,9 +337,10 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
         const int page = u == 0 ? pg0[j] : row[j];
         if (page < 0 || page >= a.num_pages) continue;
         const int y = (page * a.Hkv + g) * a.P;
+        const int yv = KV8 ? (page * a.Hkv + g) * D : y;  // FP8 V: [page][h][d][P]
         for (int hf = 0; hf < Cfg::kHalves; ++hf) {
           tc::tma_prefetch_2d(&maps.k, hf * 64, y);
-          tc::tma_prefetch_2d(&maps.v, hf * 64, y);
+          tc::tma_prefetch_2d(&maps.v, hf * 64, yv);
         }
       }
     }
@@ -424,7 +443,15 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
         const uint32_t qbytes = seg_first ? (uint32_t)(G * D * 2) : 0u;
         // masked variant: the (sequence, position) of each slot of the block's pages
         const uint32_t cbytes = (MASK && rows > 0) ? (uint32_t)(2 * npg * a.P * 4) : 0u;
-        mbar_arrive_expect_tx(&bars->full[st], 2u * Cfg::kBlk + qbytes + cbytes);
+        // FP8 pages: the K and V scales of the block's rows
+        const uint32_t sbytes = (KV8 && rows > 0) ? (uint32_t)(2 * KB * 4) : 0u;
+        mbar_arrive_expect_tx(&bars->full[st], 2u * Cfg::kBlk + qbytes + cbytes + sbytes);
+        if (KV8 && rows > 0) {
+          unsigned char *sc = stage + 2 * Cfg::kBlk + Cfg::kQ;
+          const size_t r0 = ((size_t)pgs[0] * a.Hkv + pit.g) * KB;
+          bulk_g2s(sc, a.k_scale + r0, KB * 4, &bars->full[st]);
+          bulk_g2s(sc + KB * 4, a.v_scale + r0, KB * 4, &bars->full[st]);
+        }
         if (MASK && rows > 0) {
           unsigned char *cells = stage + 2 * Cfg::kBlk + Cfg::kQ;
 #pragma unroll
@@ -435,9 +462,16 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
             bulk_g2s(cells + KB * 4 + j * a.P * 4, a.cell_pos + slot0, a.P * 4, &bars->full[st]);
           }
         }
+        if (KV8) {
+          // one page per block: K rows [128][128 B], V transposed [128 dims][128 B]
+          const int yk = rows > 0 ? ys[0] : oob_row;
+          const int yv = rows > 0 ? (pgs[0] * a.Hkv + pit.g) * D : a.num_pages * a.Hkv * D;
+          tc::tma_load_2d(stage, &maps.k, 0, yk, &bars->full[st]);
+          tc::tma_load_2d(stage + Cfg::kBlk, &maps.v, 0, yv, &bars->full[st]);
+        }
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          if (j >= pages_per_block) break;
+          if (KV8 || j >= pages_per_block) break;
           // pages past the sequence (or a skipped block) load the zero-filled tail of the map
           const int y = rows > 0 ? ys[j] : oob_row;
           for (int hf = 0; hf < Cfg::kHalves; ++hf) {
@@ -662,13 +696,27 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
       // ldmatrix x4 row addresses: matrix = lane / 8 -> (key half, dim half)
       const int lm_key = key_base + ((lane >> 4) << 3) + (lane & 7);
       const int lm_chunk = (lane >> 3) & 1;
+      if (KV8) {
+        // K codes [key][128 B], 128-byte swizzle: this lane's key of each 8-key tile,
+        // dims 16ks + 2cq (+1) and 16ks + 8 + 2cq (+1) -- the B fragment, widened
 #pragma unroll
-      for (int ks = 0; ks < KSTEPS; ++ks) {
-        const int box = ks >> 2, chunk = (ks & 3) * 2 + lm_chunk;
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(sK + box * kBox + sw128(lm_key, chunk), b0, b1, b2, b3);
-        mma16816(s[0], qa[ks][0], 0u, qa[ks][1], 0u, b0, b1);
-        mma16816(s[1], qa[ks][0], 0u, qa[ks][1], 0u, b2, b3);
+        for (int ks = 0; ks < KSTEPS; ++ks)
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const int key = key_base + t * 8 + hr;
+            const unsigned char *row = stage + key * 128 + ((ks ^ (key & 7)) << 4);
+            mma16816(s[t], qa[ks][0], 0u, qa[ks][1], 0u, e4m3x2_to_h2(lds_u16(row + 2 * cq)),
+                     e4m3x2_to_h2(lds_u16(row + 8 + 2 * cq)));
+          }
+      } else {
+#pragma unroll
+        for (int ks = 0; ks < KSTEPS; ++ks) {
+          const int box = ks >> 2, chunk = (ks & 3) * 2 + lm_chunk;
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(sK + box * kBox + sw128(lm_key, chunk), b0, b1, b2, b3);
+          mma16816(s[0], qa[ks][0], 0u, qa[ks][1], 0u, b0, b1);
+          mma16816(s[1], qa[ks][0], 0u, qa[ks][1], 0u, b2, b3);
+        }
       }
       // ---- online softmax on the fragment: this lane has keys 2cq, 2cq+1 (+8) of head hr
       float x[4];
@@ -682,7 +730,9 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
             const int *cs = reinterpret_cast<const int *>(stage + 2 * Cfg::kBlk + Cfg::kQ);
             ok = ok && cs[key_base + kk] == cit.seq && cs[KB + key_base + kk] <= cit.pos;
           }
-          x[t * 2 + e] = ok ? s[t][e] * a.scale_log2 : -INFINITY;
+          float sv = s[t][e];
+          if (KV8) sv *= reinterpret_cast<const float *>(stage + 2 * Cfg::kBlk + Cfg::kQ)[key_base + kk];
+          x[t * 2 + e] = ok ? sv * a.scale_log2 : -INFINITY;
         }
       const float xm = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
       if (__any_sync(0xffffffffu, xm > m_run + kDecRescale)) {
@@ -705,13 +755,42 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
       for (int j = 0; j < 4; ++j) p[j] = exp2_approx(x[j] - m_use);  // -inf -> 0
       l_part += (p[0] + p[1]) + (p[2] + p[3]);
       // P as the A fragment of the PV product (k = the warp's 16 keys; rows 8..15 zero)
-      const uint32_t pa0 = pack_h2(p[0], p[1]), pa2 = pack_h2(p[2], p[3]);
+      uint32_t pa0, pa2;
+      if (KV8) {
+        // fold each key's V scale into P (a key past the valid ones contributes 0)
+        const float *vsc = reinterpret_cast<const float *>(stage + 2 * Cfg::kBlk + Cfg::kQ) + KB;
+        float pv[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int kk = (j >> 1) * 8 + 2 * cq + (j & 1);
+          pv[j] = kk < nr ? p[j] * vsc[key_base + kk] : 0.f;
+        }
+        pa0 = pack_h2(pv[0], pv[1]);
+        pa2 = pack_h2(pv[2], pv[3]);
+      } else {
+        pa0 = pack_h2(p[0], p[1]);
+        pa2 = pack_h2(p[2], p[3]);
+      }
       // V rows past the valid keys may hold stale data or NaN: zero them (0 * NaN)
       if (nr < kKeysPerWarp) {
-        for (int r = key_base + nr + (lane >> 3); r < key_base + kKeysPerWarp; r += 4)
-          for (int hf = 0; hf < Cfg::kHalves; ++hf)
-            reinterpret_cast<uint4 *>(stage + Cfg::kBlk + hf * kBox + r * 128)[lane & 7] =
-                make_uint4(0, 0, 0, 0);
+        if (KV8) {
+          // V transposed: the warp's 16 keys are one 16-byte chunk of every dim row
+          for (int r = lane; r < D; r += 32) {
+            uint4 *c = reinterpret_cast<uint4 *>(stage + Cfg::kBlk + r * 128 +
+                                                 (((key_base >> 4) ^ (r & 7)) << 4));
+            uint4 x4 = *c;
+            unsigned char *b = reinterpret_cast<unsigned char *>(&x4);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (j >= nr) b[j] = 0;
+            *c = x4;
+          }
+        } else {
+          for (int r = key_base + nr + (lane >> 3); r < key_base + kKeysPerWarp; r += 4)
+            for (int hf = 0; hf < Cfg::kHalves; ++hf)
+              reinterpret_cast<uint4 *>(stage + Cfg::kBlk + hf * kBox + r * 128)[lane & 7] =
+                  make_uint4(0, 0, 0, 0);
+        }
         __syncwarp();
         zeroed = true;
       }
@@ -736,14 +815,27 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
       // ---- O += P V, 8 dims per tile; ldmatrix.trans gives the V fragments
       const int lt_key = key_base + (((lane >> 3) & 1) << 3) + (lane & 7);
       const int lt_tile = lane >> 4;
+      if (KV8) {
+        // V codes transposed [dim][128 B of keys]: this lane's dim of each 8-dim tile,
+        // keys 2cq (+1) and 8 + 2cq (+1) of the warp's 16 -- the B fragment, widened
 #pragma unroll
-      for (int t = 0; t < NT; t += 2) {
-        const int dchunk = t + lt_tile;  // 16-byte chunk = 8-dim tile
-        const int box = dchunk >> 3, chunk = dchunk & 7;
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(sV + box * kBox + sw128(lt_key, chunk), b0, b1, b2, b3);
-        mma16816(o[t], pa0, 0u, pa2, 0u, b0, b1);
-        mma16816(o[t + 1], pa0, 0u, pa2, 0u, b2, b3);
+        for (int t = 0; t < NT; ++t) {
+          const int dim = t * 8 + hr;
+          const unsigned char *row =
+              stage + Cfg::kBlk + dim * 128 + (((key_base >> 4) ^ (dim & 7)) << 4);
+          mma16816(o[t], pa0, 0u, pa2, 0u, e4m3x2_to_h2(lds_u16(row + 2 * cq)),
+                   e4m3x2_to_h2(lds_u16(row + 8 + 2 * cq)));
+        }
+      } else {
+#pragma unroll
+        for (int t = 0; t < NT; t += 2) {
+          const int dchunk = t + lt_tile;  // 16-byte chunk = 8-dim tile
+          const int box = dchunk >> 3, chunk = dchunk & 7;
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(sV + box * kBox + sw128(lt_key, chunk), b0, b1, b2, b3);
+          mma16816(o[t], pa0, 0u, pa2, 0u, b0, b1);
+          mma16816(o[t + 1], pa0, 0u, pa2, 0u, b2, b3);
+        }
       }
     }
     if (zeroed) fence_proxy_async();  // generic writes before async copies refill the stage
@@ -916,19 +1008,19 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
   }
 }
 
-template <int D, int G, bool MASK>
+template <int D, int G, bool MASK, bool KV8>
 static cudaError_t launch_decode_t(const AttnArgs &a, int num_sms, const AttnMaps *maps,
                                    cudaStream_t s) {
-  using Cfg = DecCfg<D, G, MASK>;
+  using Cfg = DecCfg<D, G, MASK, KV8>;
   static bool attr_set = false;
   if (!attr_set) {
     // setmaxnreg.inc can only draw on registers the block was launched with: refuse to
     // launch (rather than wait forever) if the compiled allocation does not cover the split
     cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, k_decode<D, G, MASK>);
+    cudaError_t e = cudaFuncGetAttributes(&fa, k_decode<D, G, MASK, KV8>);
     if (e != cudaSuccess) return e;
     if (fa.numRegs * kDecThreads < kDecRegsSplitTotal) return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(k_decode<D, G, MASK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(k_decode<D, G, MASK, KV8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Cfg::kSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
@@ -943,17 +1035,25 @@ static cudaError_t launch_decode_t(const AttnArgs &a, int num_sms, const AttnMap
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_decode<D, G, MASK>, a, *maps);
+  return cudaLaunchKernelEx(&cfg, k_decode<D, G, MASK, KV8>, a, *maps);
 }
 
 cudaError_t launch_decode(const AttnArgs &a, int num_sms, const void *tmaps, cudaStream_t s) {
   const AttnMaps *maps = static_cast<const AttnMaps *>(tmaps);
   const int G = a.Hq / a.Hkv;
   const bool masked = a.cell_seq != nullptr;
+  if (a.k_scale) {  // FP8 pages: page size 128, d 128
+    if (a.D != 128 || a.P != 128) return cudaErrorInvalidValue;
+    if (G == 1) return launch_decode_t<128, 1, false, true>(a, num_sms, maps, s);
+    if (G == 2) return launch_decode_t<128, 2, false, true>(a, num_sms, maps, s);
+    if (G == 4) return launch_decode_t<128, 4, false, true>(a, num_sms, maps, s);
+    if (G == 8) return launch_decode_t<128, 8, false, true>(a, num_sms, maps, s);
+    return cudaErrorInvalidValue;
+  }
 #define PA_DEC_CASE(DD, GG)                                                           \
   if (a.D == DD && G == GG)                                                           \
-    return masked ? launch_decode_t<DD, GG, true>(a, num_sms, maps, s)                \
-                  : launch_decode_t<DD, GG, false>(a, num_sms, maps, s);
+    return masked ? launch_decode_t<DD, GG, true, false>(a, num_sms, maps, s)         \
+                  : launch_decode_t<DD, GG, false, false>(a, num_sms, maps, s);
   PA_DEC_CASE(128, 1) PA_DEC_CASE(128, 2) PA_DEC_CASE(128, 4) PA_DEC_CASE(128, 8)
   PA_DEC_CASE(64, 1) PA_DEC_CASE(64, 2) PA_DEC_CASE(64, 4) PA_DEC_CASE(64, 8)
 #undef PA_DEC_CASE

@@ -67,6 +67,65 @@ __global__ void k_copy_pages(const int32_t *__restrict__ src, const int32_t *__r
   }
 }
 
+// FP8 E4M3 code of a binary32 value: nearest, ties to even, saturating at +-448.
+// The same value goes into both halves of the pair, so the byte order of the pair
+// does not matter.
+__device__ __forceinline__ uint8_t f32_to_e4m3(float x) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %1;" : "=h"(r) : "f"(x));
+  return static_cast<uint8_t>(r & 0xFF);
+}
+
+// Quantising reshape-and-cache into FP8 pages (one warp per (token, KV head) row):
+// scale = amax / 448 over the row (1 for an all-zero row), code = E4M3(x / scale).
+// K rows go to k8 [page][h][offset][d]; V rows to v8t [page][h][d][offset]
+// (transposed inside each (page, head) block); the scales to [page][h][offset].
+__global__ void k_append_fp8(const uint16_t *__restrict__ k, const uint16_t *__restrict__ v,
+                             const int64_t *__restrict__ slot, int T, uint8_t *__restrict__ k8,
+                             uint8_t *__restrict__ v8t, float *__restrict__ ks,
+                             float *__restrict__ vs, int num_pages, int Hkv, int P, int d,
+                             int *err) {
+  const int lane = threadIdx.x & 31;
+  const long long nw = (long long)gridDim.x * blockDim.x / 32;
+  for (long long r = ((long long)blockIdx.x * blockDim.x + threadIdx.x) / 32;
+       r < (long long)T * Hkv; r += nw) {
+    const int t = (int)(r / Hkv), h = (int)(r % Hkv);
+    const int64_t sl = slot[t];
+    if (sl < 0) continue;
+    if (sl >= (int64_t)num_pages * P) {
+      if (err && lane == 0) atomicOr(err, PA_ERR_SLOT_RANGE);
+      continue;
+    }
+    const int64_t page = sl / P, off = sl % P;
+    const size_t row = ((size_t)page * Hkv + h) * P + off;
+    for (int which = 0; which < 2; ++which) {
+      const uint16_t *src = (which ? v : k) + ((size_t)t * Hkv + h) * d;
+      float x[4];
+      float amax = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int i = lane + 32 * j;
+        x[j] = i < d ? __half2float(__ushort_as_half(src[i])) : 0.f;
+        amax = fmaxf(amax, fabsf(x[j]));
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      const float scale = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int i = lane + 32 * j;
+        if (i >= d) break;
+        const uint8_t c = f32_to_e4m3(__fdiv_rn(x[j], scale));
+        if (which == 0)
+          k8[row * d + i] = c;
+        else
+          v8t[(((size_t)page * Hkv + h) * d + i) * P + off] = c;
+      }
+      if (lane == 0) (which ? vs : ks)[row] = scale;
+    }
+  }
+}
+
 __global__ void k_append(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
                          const int64_t *__restrict__ slot, int T, uint4 *__restrict__ kp,
                          uint4 *__restrict__ vp, int num_pages, int Hkv, int P, int chunks_per_row,

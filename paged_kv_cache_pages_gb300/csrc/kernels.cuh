@@ -10,6 +10,9 @@ __global__ void k_expand(const int32_t *seq_pt, int n_seq, int max_pages, const 
                          int64_t *slot, int *err);
 __global__ void k_append(const uint4 *k, const uint4 *v, const int64_t *slot, int T, uint4 *kp,
                          uint4 *vp, int num_pages, int Hkv, int P, int chunks_per_row, int *err);
+__global__ void k_append_fp8(const uint16_t *k, const uint16_t *v, const int64_t *slot, int T,
+                             uint8_t *k8, uint8_t *v8t, float *ks, float *vs, int num_pages,
+                             int Hkv, int P, int d, int *err);
 __global__ void k_copy_pages(const int32_t *src, const int32_t *dst, int n, uint4 *kp, uint4 *vp,
                              int num_pages, long long page_units, int *err);
 __global__ void k_validate(const int32_t *tpt, int max_pages, const int32_t *kv, int T, int P,
@@ -34,6 +37,8 @@ struct AttnArgs {
   // masked decode (unified-span baseline) only, else null: (sequence, position) of
   // every slot of the pool and of every token
   const int32_t *cell_seq, *cell_pos, *tok_seq, *tok_pos;
+  // FP8 pages only, else null: the binary32 scale of every cached (page, head, row)
+  const float *k_scale, *v_scale;
 };
 
 // Decode: split-KV over all SMs plus the log-sum-exp reduce.  Returns a

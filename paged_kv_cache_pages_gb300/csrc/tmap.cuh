@@ -15,5 +15,8 @@ struct AttnMaps {
 };
 
 int encode_attn_maps(const AttnArgs &a, AttnMaps *m);
+// FP8 pages (page size 128, d 128): K {d bytes, rows}, V transposed {P bytes, rows},
+// both in 128 x 128-byte boxes with 128-byte swizzle; q as above.
+int encode_attn_maps_fp8(const AttnArgs &a, AttnMaps *m);
 
 }  // namespace pa

@@ -118,6 +118,7 @@ def span(reps: int):
     q = torch.from_numpy(c.q.view(np.float16)).to(dev)
     out = torch.empty_like(q)
     ws = pa.new_workspace(c.T, c.Hq, c.Hkv, c.d, dev)
+    pa.plan_decode(tpt, kv, c.Hq, c.Hkv, c.P, c.d, ws)
     ms = _time(lambda: pa.masked_decode(q, kp, vp, tpt, kv, c.scale, cs, cp, ts, tp, out, ws),
                reps)
     if pa.read_error(ws):

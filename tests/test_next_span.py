@@ -107,6 +107,7 @@ def run_masked(pa, case, kp, vp):
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
     out = torch.empty((case.T, case.Hq, case.d), dtype=torch.float16, device=dev)
     ws = pa.new_workspace(case.T, case.Hq, case.Hkv, case.d, dev)
+    pa.plan_decode(t(tpt), t(kv), case.Hq, case.Hkv, case.P, case.d, ws)
     pa.masked_decode(t(case.q.view(np.float16)), t(kp.view(np.float16)), t(vp.view(np.float16)),
                      t(tpt), t(kv), case.scale, t(cs), t(cp), t(ts), t(tp), out, ws)
     torch.cuda.synchronize()
