@@ -35,14 +35,16 @@ METRIC = "decode KV GB/s + prefill TFLOP/s, Qwen3-8B-shape paged attn, 8×16K, 1
 # traffic null.  k_prefill: mean of the 65 launches of one 8x16K step (launch list of
 # `bench.py --steps 2 --warmup 3 --no-cpu-baseline`); k_decode: one decode_8seq launch
 # (`profile_case decode`, cold L2); k_decode_span: one masked launch of
-# `profile_case span`; k_copy_pages: one launch of `profile_case copy`
+# `profile_case span`; k_decode_fp8: one FP8 launch of `profile_case fp8`;
+# k_copy_pages: one launch of `profile_case copy`
 # (writes still in L2 at the end of the launch are not counted).  Summaries and
 # commands: profiles/.
 TRAFFIC = {
-    "k_prefill": {"bytes": 640.0e6, "files": ["k_prefill.cu"], "digest": "0613826f8111c26b"},
-    "k_decode": {"bytes": 86.01e6, "files": ["k_decode.cu"], "digest": "71e65c5d4c64acc7"},
-    "k_decode_span": {"bytes": 116.26e6, "files": ["k_decode.cu"], "digest": "71e65c5d4c64acc7"},
-    "k_copy_pages": {"bytes": 488.11e6, "files": ["k_small.cu"], "digest": "4e74b422bc424659"},
+    "k_prefill": {"bytes": 641.9e6, "files": ["k_prefill.cu"], "digest": "ac285c83b01609e3"},
+    "k_decode": {"bytes": 86.06e6, "files": ["k_decode.cu"], "digest": "a96899430d392e78"},
+    "k_decode_span": {"bytes": 115.90e6, "files": ["k_decode.cu"], "digest": "a96899430d392e78"},
+    "k_decode_fp8": {"bytes": 43.67e6, "files": ["k_decode.cu"], "digest": "a96899430d392e78"},
+    "k_copy_pages": {"bytes": 488.07e6, "files": ["k_small.cu"], "digest": "e655523236e56b60"},
 }
 _TRAFFIC_HEADERS = ["common.cuh", "tc.cuh", "tmap.cuh", "kernels.cuh"]
 
@@ -503,7 +505,7 @@ def bench_fp8_decode(pa, torch, db, steps, warmup, world, hbm, f16_ms_per_layer)
             "speedup_vs_f16": round(f16_ms_per_layer / ms_layer, 2),
             "roofline": {"bound": "hbm", "kernel": "k_decode (FP8 pages)",
                          "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
-                         "frac": round(gbs / hbm, 4), "traffic": None},
+                         "frac": round(gbs / hbm, 4), "traffic": traffic_of("k_decode_fp8")},
             "timing": "CUDA graph of one plan and 36 FP8 decode launches (one per layer)"}
 
 

@@ -12,6 +12,9 @@
   python -m paged_kv_cache_pages_gb300.profile_case span [--reps R]
       the unified-span baseline on the decode layer: every token reads the whole
       pool under a per-cell mask (one plan + masked decode per call).
+  python -m paged_kv_cache_pages_gb300.profile_case fp8 [--reps R] [--pools N]
+      the decode layer over FP8 pages (every cached row quantised by the
+      library's append), N pool copies in turn (default 8).
   python -m paged_kv_cache_pages_gb300.profile_case copy [--reps R]
       page copy of copy-on-write forks: 512 of 1280 pages (8 KV heads x 128 rows
       x d 128, K and V) copied to 512 others per call.
@@ -128,6 +131,42 @@ def span(reps: int):
           f"({c.num_pages} pages read by each of {c.T} tokens)")
 
 
+def fp8(reps: int, n_pools: int):
+    c = workloads.decode(0)
+    dev = "cuda"
+    tpt, kv, _ = pa.expand_ubatch(
+        torch.from_numpy(c.seq_page_table()).to(dev), torch.from_numpy(c.tok_seq).to(dev),
+        torch.from_numpy(c.tok_pos).to(dev), c.P)
+    rows_k, rows_v, slots = [], [], []
+    for s, pages in enumerate(c.seq_pages):
+        L = int(c.seq_len[s])
+        pos = np.arange(L)
+        slots.append(np.asarray(pages, np.int64)[pos // c.P] * c.P + pos % c.P)
+        rows_k.append(c.k_ctx[s][:L])
+        rows_v.append(c.v_ctx[s][:L])
+    base = pa.new_fp8_pool(c.num_pages, c.Hkv, c.P, c.d, dev)
+    pa.kv_append_fp8(torch.from_numpy(np.concatenate(rows_k).view(np.float16)).to(dev),
+                     torch.from_numpy(np.concatenate(rows_v).view(np.float16)).to(dev),
+                     torch.from_numpy(np.concatenate(slots)).to(dev), *base)
+    pools = [base] + [tuple(t.clone() for t in base) for _ in range(n_pools - 1)]
+    q = torch.from_numpy(c.q.view(np.float16)).to(dev)
+    out = torch.empty_like(q)
+    ws = pa.new_workspace(c.T, c.Hq, c.Hkv, c.d, dev)
+    pa.plan_decode(tpt, kv, c.Hq, c.Hkv, c.P, c.d, ws)
+    turn = [0]
+
+    def fn():
+        p_ = pools[turn[0] % len(pools)]
+        turn[0] += 1
+        pa.decode_fp8(q, *p_, tpt, kv, c.scale, out, ws)
+
+    ms = _time(fn, reps)
+    if pa.read_error(ws):
+        raise SystemExit("device error word set")
+    nbytes = float(c.seq_len.astype(np.int64).sum()) * c.Hkv * (2 * c.d + 8)
+    print(f"fp8: {ms * 1e3:.1f} us/call {nbytes / ms / 1e6:.1f} GB/s ({len(pools)} pools in turn)")
+
+
 def copy(reps: int):
     dev = "cuda"
     N, Hkv, P, d, n = 1280, 8, 128, 128, 512
@@ -144,7 +183,7 @@ def copy(reps: int):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["prefill", "decode", "copy", "span"])
+    ap.add_argument("case", choices=["prefill", "decode", "copy", "span", "fp8"])
     ap.add_argument("--ubatch", type=int, default=48)
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--pools", type=int, default=8)
@@ -155,6 +194,8 @@ def main():
         decode(a.reps, a.pools)
     elif a.case == "span":
         span(a.reps)
+    elif a.case == "fp8":
+        fp8(a.reps, a.pools)
     else:
         copy(a.reps)
 

@@ -193,3 +193,14 @@ def test_fork_copy_append_attention(pa):
     assert_attn_close(out.float().cpu().numpy(), ref, "fork")
     # the two sequences share their first 37 keys and differ only in the last one
     assert not np.allclose(ref[0], ref[1])
+
+
+@pytest.mark.gpu
+def test_copy_pages_of_nothing_is_a_no_op(pa):
+    import torch
+    k = torch.zeros((4, 2, 16, 64), dtype=torch.float16, device="cuda")
+    v = torch.zeros_like(k)
+    e = torch.empty(0, dtype=torch.int32, device="cuda")
+    pa.copy_pages(e, e, k, v)
+    torch.cuda.synchronize()
+    assert not k.any() and not v.any()

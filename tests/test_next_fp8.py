@@ -180,3 +180,54 @@ def test_decode_fp8_matches_oracle(pa, Hq, Hkv):
     torch.cuda.synchronize()
     assert pa.read_error(ws) == 0
     assert_attn_close(out.float().cpu().numpy(), want, f"fp8 G={Hq // Hkv}")
+
+
+def _fp8_setup(pa, seed=50, Hq=32, Hkv=8):
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(100, 2000, 4)
+    case = workloads.build_case("fp8e", seed, lens, [(s, int(L) - 1) for s, L in enumerate(lens)],
+                                P=128, Hq=Hq, Hkv=Hkv, d=128)
+    k, v, slot = fill_slots(case)
+    dev = "cuda"
+    pool = pa.new_fp8_pool(case.num_pages, Hkv, 128, 128, dev)
+    pa.kv_append_fp8(torch.from_numpy(k.view(np.float16)).to(dev),
+                     torch.from_numpy(v.view(np.float16)).to(dev),
+                     torch.from_numpy(slot).to(dev), *pool)
+    tpt, kv, _ = oracle.expand_ubatch(case.seq_page_table(), case.tok_seq, case.tok_pos, 128)
+    return case, pool, tpt, kv
+
+
+def _fp8_run(pa, case, pool, tpt, kv):
+    dev = "cuda"
+    q = torch.from_numpy(case.q.view(np.float16)).to(dev)
+    out = torch.full_like(q, float("nan"))
+    ws = pa.new_workspace(case.T, case.Hq, case.Hkv, 128, dev)
+    tpt_d, kv_d = torch.from_numpy(tpt).to(dev), torch.from_numpy(kv).to(dev)
+    pa.plan_decode(tpt_d, kv_d, case.Hq, case.Hkv, 128, 128, ws)
+    pa.decode_fp8(q, *pool, tpt_d, kv_d, case.scale, out, ws)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy(), pa.read_error(ws)
+
+
+@pytest.mark.gpu
+def test_decode_fp8_bad_page_and_empty_rows(pa):
+    case, pool, tpt, kv = _fp8_setup(pa)
+    tpt = tpt.copy()
+    kv = kv.copy()
+    tpt[1, 0] = case.num_pages + 3  # out of the pool: flagged, that block skipped, no fault
+    kv[2] = 0                       # no key: a zero row
+    out, err = _fp8_run(pa, case, pool, tpt, kv)
+    assert err & pa.PA_ERR_PAGE_RANGE
+    assert np.all(out[2] == 0.0)
+    # the context stays usable and the untouched tokens are right
+    tpt2, kv2 = _fp8_setup(pa)[2:]
+    out2, err2 = _fp8_run(pa, case, pool, tpt2, kv2)
+    assert err2 == 0 and np.all(np.isfinite(out2))
+
+
+@pytest.mark.gpu
+def test_decode_fp8_is_bitwise_deterministic(pa):
+    case, pool, tpt, kv = _fp8_setup(pa, seed=51)
+    a, _ = _fp8_run(pa, case, pool, tpt, kv)
+    b, _ = _fp8_run(pa, case, pool, tpt, kv)
+    assert np.array_equal(a, b)

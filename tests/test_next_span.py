@@ -140,3 +140,16 @@ def test_masked_decode_long_tail_sampled(pa):
     toks = np.array([0, 9, int(np.argmax(case.seq_len)), int(np.argmin(case.seq_len))], np.int32)
     ref = oracle.paged_attention(case.q, kp, vp, tpt0, kv0, case.scale, toks)
     assert_attn_close(got[toks], ref, "masked long tail")
+
+
+@pytest.mark.gpu
+def test_masked_decode_padding_token_gets_zero_row(pa):
+    case = workloads.tiny(0)
+    case.tok_seq = case.tok_seq.copy()
+    case.tok_seq[3] = -1  # a padding token: kv_len 0 in the span view, zero output
+    _, kp, vp = paged_ref(workloads.tiny(0))
+    got, (tpt, kv, cs, cp, ts, tp) = run_masked(pa, case, kp, vp)
+    assert kv[3] == 0 and np.all(got[3] == 0.0)
+    mref = oracle.masked_attention(case.q, kp, vp, tpt, kv, case.scale, cs, cp, ts, tp)
+    from tests._gpu import assert_attn_close
+    assert_attn_close(got, mref, "masked with padding")
