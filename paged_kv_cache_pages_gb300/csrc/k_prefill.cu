@@ -278,25 +278,35 @@ k_prefill(AttnArgs a, const __grid_constant__ AttnMaps maps) {
     constexpr uint32_t idPV = tc::idesc_f16(128, D, true);
     const uint32_t sQ0 = smem_u32(smem + Cfg::kQ0), sQ1 = smem_u32(smem + Cfg::kQ1);
     const uint32_t sK = smem_u32(smem + Cfg::kK), sV = smem_u32(smem + Cfg::kV);
+    // Descriptors of the operand tiles, made once: a k-step moves the start address
+    // (bits 0-13, in 16-byte units) by a constant, and every shared-memory address
+    // here is below 256 KB, so adding to the descriptor never carries out of the field.
+    static_assert(kPfStages == 2, "two K/V stages");
+    const uint64_t dQ0 = tc::sdesc_sw128(sQ0, 16, 1024), dQ1 = tc::sdesc_sw128(sQ1, 16, 1024);
+    const uint64_t dK0 = tc::sdesc_sw128(sK, 16, 1024);
+    const uint64_t dK1 = tc::sdesc_sw128(sK + Cfg::kTile, 16, 1024);
+    const uint64_t dV0 = tc::sdesc_sw128(sV, kBoxBytes, 1024);
+    const uint64_t dV1 = tc::sdesc_sw128(sV + Cfg::kTile, kBoxBytes, 1024);
     auto issue_S = [&](int i, int st) {
       const uint32_t d = tmem + i * 128;
-      const uint32_t kb = sK + st * Cfg::kTile;
+      const uint64_t a0 = i ? dQ1 : dQ0, b0 = st ? dK1 : dK0;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk / 4) * kBoxBytes + (kk % 4) * 32;
-        tc::mma_ss(d, tc::sdesc_sw128((i ? sQ1 : sQ0) + off, 16, 1024),
-                   tc::sdesc_sw128(kb + off, 16, 1024),
-                   idS, kk > 0 ? 1u : 0u);
+        const uint32_t off16 = ((kk / 4) * kBoxBytes + (kk % 4) * 32) >> 4;
+        if (kk == 0)
+          tc::mma_ss_first(d, a0, b0, idS);
+        else
+          tc::mma_ss_acc(d, a0 + off16, b0 + off16, idS);
       }
     };
     auto issue_PV = [&](int i, int st, bool acc) {
       const uint32_t d = tmem + 256 + i * D;
       const uint32_t p = tmem + i * 128;
-      const uint32_t vb = sV + st * Cfg::kTile;
+      const uint64_t b0 = st ? dV1 : dV0;
+      tc::mma_ts(d, p, b0, idPV, acc ? 1u : 0u);
 #pragma unroll
-      for (int kk = 0; kk < KB / 16; ++kk)
-        tc::mma_ts(d, p + kk * 8, tc::sdesc_sw128(vb + kk * 2048, kBoxBytes, 1024), idPV,
-                   (acc || kk > 0) ? 1u : 0u);
+      for (int kk = 1; kk < KB / 16; ++kk)
+        tc::mma_ts_acc(d, p + kk * 8, b0 + (uint32_t)((kk * 2048) >> 4), idPV);
     };
     const bool leader = lane == 0;
     uint32_t it = 0, sc = 0;
