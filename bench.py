@@ -40,11 +40,11 @@ METRIC = "decode KV GB/s + prefill TFLOP/s, Qwen3-8B-shape paged attn, 8×16K, 1
 # (writes still in L2 at the end of the launch are not counted).  Summaries and
 # commands: profiles/.
 TRAFFIC = {
-    "k_prefill": {"bytes": 641.9e6, "files": ["k_prefill.cu"], "digest": "ac285c83b01609e3"},
-    "k_decode": {"bytes": 86.06e6, "files": ["k_decode.cu"], "digest": "a96899430d392e78"},
-    "k_decode_span": {"bytes": 115.90e6, "files": ["k_decode.cu"], "digest": "a96899430d392e78"},
-    "k_decode_fp8": {"bytes": 43.67e6, "files": ["k_decode.cu"], "digest": "a96899430d392e78"},
-    "k_copy_pages": {"bytes": 488.07e6, "files": ["k_small.cu"], "digest": "e655523236e56b60"},
+    "k_prefill": {"bytes": 667.9e6, "files": ["k_prefill.cu"], "digest": "4d23de7efd7ab54d"},
+    "k_decode": {"bytes": 85.97e6, "files": ["k_decode.cu"], "digest": "20d219a4606a760a"},
+    "k_decode_span": {"bytes": 116.20e6, "files": ["k_decode.cu"], "digest": "20d219a4606a760a"},
+    "k_decode_fp8": {"bytes": 43.67e6, "files": ["k_decode.cu"], "digest": "20d219a4606a760a"},
+    "k_copy_pages": {"bytes": 488.18e6, "files": ["k_small.cu"], "digest": "73fcec2b7b03f171"},
 }
 _TRAFFIC_HEADERS = ["common.cuh", "tc.cuh", "tmap.cuh", "kernels.cuh"]
 
