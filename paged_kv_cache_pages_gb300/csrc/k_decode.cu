@@ -2,13 +2,13 @@
 //
 // The work is the planned decode tokens.  Each (token i, KV head g) owns
 // ceil(kv_len / 128) key blocks ("units"); all units of all (i, g) are laid end
-// to end and cut into gridDim.x equal contiguous ranges, one per CTA (one CTA
-// per SM), so every SM streams the same number of KV bytes whatever the length
-// mix.  A (i, g) whose units fall in one CTA is finished there; one that spans
-// CTAs leaves one partial (m, l, acc) per CTA and the CTA that finishes last
-// combines them (the partition + reduce scheme of the CacheFlow page, section
-// 核心架构 3, "Paged Attention V2", fused into one launch: an arrival counter
-// decides who combines, nobody waits).
+// to end and cut into C = min(gridDim.x, units) equal contiguous ranges, one per
+// CTA (one CTA per SM), so every SM streams the same number of KV bytes whatever
+// the length mix.  A (i, g) whose units fall in one CTA is finished there; one
+// that spans CTAs leaves one partial (m, l, acc) per CTA and the CTA whose part
+// arrives last combines them (the partition + reduce scheme of the CacheFlow page,
+// section 核心架构 3, "Paged Attention V2", fused into one launch: an
+// acquire/release arrival counter decides who combines, nobody waits).
 //
 // CTA = 12 warps.  One producer thread streams, for every unit, the 128 K rows
 // and 128 V rows of the block as 128-byte-swizzled TMA boxes (one per page and
@@ -20,11 +20,18 @@
 // f16 inputs, f32 accumulation): S = Q K^T for the warp's 16 keys, then
 // O += P V with P taken straight from the S registers.  The softmax is online
 // with quad shuffles and a lazy running max; warps merge at segment ends.  A
-// combining warp folds the splits of other CTAs.  Scalar FP32 FMAs plus f16 ->
-// f32 conversions could not keep up with HBM on this part (about 3200 issue
-// cycles of math per 128-key block against about 3000 cycles of HBM time),
-// which is why the two small contractions use the tensor path; tcgen05 and
-// TMEM stay with the prefill tiles.
+// combining warp folds the splits that end inside the CTA's range and, for the
+// split that ends it, fetches the other CTAs' parts into shared memory as soon as
+// they are published.  Scalar FP32 FMAs plus f16 -> f32 conversions could not
+// keep up with HBM on this part (about 3200 issue cycles of math per 128-key
+// block against about 3000 cycles of HBM time), which is why the two small
+// contractions use the tensor path; tcgen05 and TMEM stay with the prefill tiles.
+//
+// The launch is a programmatic dependent of the kernel before it: before waiting
+// for it, the producer asks L2 for the CTA's first blocks, and right after the
+// wait the grid releases the next launch, whose CTAs then take SMs as this grid's
+// CTAs leave them.  Two variants share the engine: MASK (per-slot sequence and
+// position mask: the unified-span baseline) and KV8 (FP8 E4M3 pages).
 #include "kernels.cuh"
 #include "tc.cuh"
 #include "tmap.cuh"
