@@ -11,6 +11,19 @@
  * rows into their pages is the "reshape-and-cache" kernel of the CacheFlow page
  * (section 核心架构 3).
  *
+ * Entry points
+ * ------------
+ *  the path:   paged_expand_ubatch, paged_kv_append, paged_attn_plan,
+ *              paged_attn_prefill, paged_attn_decode, paged_attn_run,
+ *              paged_attn_forward, paged_attn_forward_noalloc
+ *  around it:  paged_attn_workspace_size, paged_attn_validate,
+ *              paged_attn_read_error, paged_attn_strerror, paged_attn_version,
+ *              paged_attn_set_prefill_min_run, pa_pool_* (host page pool)
+ *  beyond it:  paged_attn_plan_decode; paged_attn_masked_decode (the
+ *              unified-span baseline that paging replaces); paged_kv_append_fp8
+ *              and paged_attn_decode_fp8 (FP8 pages); paged_copy_pages and
+ *              pa_pool_fork (copy-on-write forks of shared pages)
+ *
  * Conventions shared by every call
  * --------------------------------
  *  - f16 data are IEEE binary16 values passed as uint16_t bit patterns.
