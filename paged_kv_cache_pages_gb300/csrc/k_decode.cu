@@ -1019,8 +1019,8 @@ template <int D, int G, bool MASK, bool KV8>
 static cudaError_t launch_decode_t(const AttnArgs &a, int num_sms, const AttnMaps *maps,
                                    cudaStream_t s) {
   using Cfg = DecCfg<D, G, MASK, KV8>;
-  static bool attr_set = false;
-  if (!attr_set) {
+  static PerDeviceOnce setup;
+  if (setup.first()) {
     // setmaxnreg.inc can only draw on registers the block was launched with: refuse to
     // launch (rather than wait forever) if the compiled allocation does not cover the split
     cudaFuncAttributes fa;
@@ -1030,7 +1030,7 @@ static cudaError_t launch_decode_t(const AttnArgs &a, int num_sms, const AttnMap
     e = cudaFuncSetAttribute(k_decode<D, G, MASK, KV8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Cfg::kSmem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    setup.mark();
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_sms);

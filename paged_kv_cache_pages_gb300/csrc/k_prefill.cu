@@ -649,8 +649,8 @@ template <int D>
 static cudaError_t launch_prefill_t(const AttnArgs &a, int num_sms, const AttnMaps *maps,
                                     cudaStream_t s) {
   using Cfg = PfCfg<D>;
-  static bool attr_set = false;
-  if (!attr_set) {
+  static PerDeviceOnce setup;
+  if (setup.first()) {
     // setmaxnreg.inc can only draw on registers the block was launched with: refuse to
     // launch (rather than wait forever) if the compiled allocation does not cover the split
     cudaFuncAttributes fa;
@@ -659,7 +659,7 @@ static cudaError_t launch_prefill_t(const AttnArgs &a, int num_sms, const AttnMa
     if (fa.numRegs * kPfThreads < kRegsSplitTotal) return cudaErrorInvalidConfiguration;
     e = cudaFuncSetAttribute(k_prefill<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    setup.mark();
   }
   k_prefill<D><<<num_sms, kPfThreads, Cfg::kSmem, s>>>(a, *maps);
   return cudaGetLastError();

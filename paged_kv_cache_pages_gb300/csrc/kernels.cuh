@@ -1,6 +1,8 @@
 // Kernel declarations and launch parameters shared by the translation units.
 #pragma once
 
+#include <atomic>
+
 #include "common.cuh"
 
 namespace pa {
@@ -21,6 +23,24 @@ __global__ void k_plan_mark(const int32_t *tpt, int max_pages, int T, unsigned c
                             WsLayout lay);
 __global__ void k_plan(const int32_t *tpt, int max_pages, const int32_t *kv, int T, int P, int Hkv,
                        int NP, int min_run, int C, unsigned char *ws, WsLayout lay);
+
+// Per-device flags of a kernel's one-time launch setup (function attributes are per
+// device).  Returns true for the first caller on the current device, which then
+// does the setup; a race makes two callers do the same idempotent setup.
+struct PerDeviceOnce {
+  std::atomic<unsigned long long> done{0};
+  bool first() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return true;
+    const unsigned long long bit = 1ull << dev;
+    return (done.load(std::memory_order_acquire) & bit) == 0;
+  }
+  void mark() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return;
+    done.fetch_or(1ull << dev, std::memory_order_release);
+  }
+};
 
 // Arguments of the attention kernels (passed by value).
 struct AttnArgs {
