@@ -192,6 +192,23 @@ __device__ __forceinline__ void consumers_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kDecWarps * 32) : "memory");
 }
 
+// Loads of the plan issued in program order at the point where they stand (volatile:
+// the compiler neither sinks them into the branch that uses them nor merges them with
+// the speculative reads made before the dependency wait), served by L2 (.cg), so a
+// line the speculative reads left in L1 is never used.
+__device__ __forceinline__ int2 ld_v2_early(const int *p) {
+  int2 r;
+  asm volatile("ld.global.cg.v2.s32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+  return r;
+}
+__device__ __forceinline__ int4 ld_v4_early(const int4 *p) {
+  int4 r;
+  asm volatile("ld.global.cg.v4.s32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
 // Arrival counters of split segments: a part is published by a release increment
 // after its partial is written; whoever sees every other part published reads them.
 __device__ __forceinline__ int ld_acquire(const int *p) {
@@ -328,20 +345,32 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
   // no result (if the append writes into a block, L2 holds the new rows; if a record
   // is stale, the prefetch is merely wasted).
   if (w == kDecWarps && lane == 0) {
+    // reads past L1 (.cg): they precede the wait and must leave no line there
     const int4 *srec = reinterpret_cast<const int4 *>(a.ws + a.lay.dec_start) + 4 * blockIdx.x;
-    const int4 s0 = srec[0], s1 = srec[1], p0 = srec[2], p1 = srec[3];
+    const int4 s0 = __ldcg(srec), s1 = __ldcg(srec + 1), p0 = __ldcg(srec + 2),
+               p1 = __ldcg(srec + 3);
     const int g = s0.y, kb = s0.z, tok = s0.w, units = s1.x;
     const int ppb = KB / a.P;  // pages per key block
-    const int pg0[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
     // a CTA without units has no record: only in-range rows are looked up
     const bool sane = tok >= 0 && tok < a.T && kb >= 0 && g >= 0 && g < a.Hkv;
-    for (int u = 0; sane && u < NS && kb + u < units; ++u) {
-      if ((kb + u + 1) * ppb > a.max_pages) break;
-      const int32_t *row = a.tpt + (size_t)tok * a.max_pages + (size_t)(kb + u) * ppb;
+    // the page ids of the next units, all requested before the first is used
+    // (single-page blocks, the usual case; wider blocks prefetch their first unit only)
+    const int nu = !sane ? 0 : ppb == 1 ? min(min(NS, units - kb), a.max_pages - kb) : 1;
+    int pid[6];
+#pragma unroll
+    for (int u = 0; u < 6; ++u) {
+      const int32_t *row = a.tpt + (size_t)tok * a.max_pages + (size_t)(kb + u);
+      pid[u] = u == 0 ? p0.x : (u < nu ? __ldcg(row) : -1);
+    }
+    const int pg0[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+    for (int u = 0; u < nu; ++u) {
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         if (j >= ppb) break;
-        const int page = u == 0 ? pg0[j] : row[j];
+        int page = pg0[j];
+#pragma unroll
+        for (int x = 1; x < 6; ++x)
+          if (u == x) page = pid[x];
         if (page < 0 || page >= a.num_pages) continue;
         const int y = (page * a.Hkv + g) * a.P;
         const int yv = KV8 ? (page * a.Hkv + g) * D : y;  // FP8 V: [page][h][d][P]
@@ -356,13 +385,27 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
   // the next kernel in the stream may be scheduled onto SMs as this grid's CTAs leave
   // them (a programmatically launched successor still waits for this grid to complete)
   asm volatile("griddepcontrol.launch_dependents;");
-  __syncthreads();
   WsHeader *hdr = reinterpret_cast<WsHeader *>(a.ws);
+  const int c = blockIdx.x;
+  // Everything the first copy needs is loaded here, at once, so that it costs one L2
+  // round trip after the wait rather than a chain of dependent ones: the header's
+  // counts (every thread) and the CTA's start record with its first page ids (the
+  // producer warp).
+  const int2 counts = ld_v2_early(&hdr->n_dec);  // (n_dec, n_units)
+  const int4 *start = reinterpret_cast<const int4 *>(a.ws + a.lay.dec_start) + 4 * c;
+  int4 start0 = make_int4(0, 0, 0, 0), start1 = start0, start2 = start0, start3 = start0;
+  if (w == kDecWarps) {
+    start0 = ld_v4_early(start);
+    start1 = ld_v4_early(start + 1);
+    start2 = ld_v4_early(start + 2);
+    start3 = ld_v4_early(start + 3);
+  }
+  __syncthreads();
   int *err = &hdr->err;
   DecView v;
   v.dec_tok = reinterpret_cast<const int *>(a.ws + a.lay.dec_tok);
   v.tok_unit_off = reinterpret_cast<const int *>(a.ws + a.lay.tok_unit_off);
-  v.n_dec = hdr->n_dec;
+  v.n_dec = counts.x;
   v.Hkv = a.Hkv;
   v.cap = a.max_pages * a.P;
   v.kv = a.kv;
@@ -371,13 +414,15 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
   float *partials = reinterpret_cast<float *>(a.ws + a.lay.partials);
   int *dec_cnt = reinterpret_cast<int *>(a.ws + a.lay.dec_cnt);
 
-  const int U = hdr->n_units;
-  const int c = blockIdx.x;
-  // decode tokens with no key (kv_len 0) own no unit: their rows are zero
-  for (int i = c; i < v.n_dec; i += gridDim.x) {
-    if (v.tok_unit_off[i + 1] != v.tok_unit_off[i]) continue;
-    uint16_t *orow = a.out + (size_t)v.dec_tok[i] * a.Hq * D;
-    for (int x = threadIdx.x; x < a.Hq * D; x += blockDim.x) orow[x] = 0;
+  const int U = counts.y;
+  // decode tokens with no key (kv_len 0) own no unit: their rows are zero (written by
+  // a warp that has no other work, off the path of the first copy)
+  if (w == kDecWarps + 2) {
+    for (int i = c; i < v.n_dec; i += gridDim.x) {
+      if (v.tok_unit_off[i + 1] != v.tok_unit_off[i]) continue;
+      uint16_t *orow = a.out + (size_t)v.dec_tok[i] * a.Hq * D;
+      for (int x = lane; x < a.Hq * D; x += 32) orow[x] = 0;
+    }
   }
   // the units go to C = min(gridDim.x, U) CTAs, each of which owns at least one
   const int C = min((int)gridDim.x, U);
@@ -385,8 +430,6 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
   const int u0 = (int)((int64_t)c * U / C), u1 = (int)((int64_t)(c + 1) * U / C);
   if (u0 >= u1) return;
   const int n = u1 - u0;
-  const int4 *start = reinterpret_cast<const int4 *>(a.ws + a.lay.dec_start) + 4 * c;
-  const int4 start0 = start[0], start1 = start[1];
 
   volatile int *abort = &bars->abort;
 
@@ -412,7 +455,7 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
         for (int j = 0; j < 8; ++j) pgs[j] = j < npg ? row[j] : -1;
       };
       {  // the first unit's page ids come with its start record
-        const int4 p0 = start[2], p1 = start[3];
+        const int4 p0 = start2, p1 = start3;
         npg = (min(KB, pit.L - pit.kb * KB) + a.P - 1) / a.P;
         pgs[0] = p0.x; pgs[1] = p0.y; pgs[2] = p0.z; pgs[3] = p0.w;
         pgs[4] = p1.x; pgs[5] = p1.y; pgs[6] = p1.z; pgs[7] = p1.w;
@@ -697,7 +740,17 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
 
     const int nr = min(max(rows - key_base, 0), kKeysPerWarp);
     bool zeroed = false;
-    if (nr > 0) {
+    // masked variant: a slice whose 16 cells all fail the mask adds exactly nothing
+    // (every probability is 0), so the warp skips it (the block is still read whole)
+    bool any_kept = true;
+    if (MASK && nr > 0) {
+      const int *cs = reinterpret_cast<const int *>(stage + 2 * Cfg::kBlk + Cfg::kQ);
+      const int kr = lane & 15;
+      const bool keep = lane < 16 && kr < nr && cs[key_base + kr] == cit.seq &&
+                        cs[KB + key_base + kr] <= cit.pos;
+      any_kept = __ballot_sync(0xffffffffu, keep) != 0u;
+    }
+    if (nr > 0 && any_kept) {
       // ---- S = Q K^T for the warp's 16 keys (two 8-key tiles), f32 accumulators
       float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
       // ldmatrix x4 row addresses: matrix = lane / 8 -> (key half, dim half)
