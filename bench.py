@@ -212,16 +212,39 @@ class PrefillBench:
             self._ubatch(d, None if events is None else events[i])
 
     def step_e2e(self):
-        """Same step from pinned host buffers: H2D of each ubatch's inputs, D2H of its output."""
+        """Same step from pinned host buffers: H2D of each ubatch's inputs, D2H of its
+        output.  The uploads run on one copy stream and the downloads on another, so the
+        copies of other ubatches overlap the attention of this one; ubatch i's kernels
+        wait (event) for its own upload, and its download waits for its kernels.  Every
+        ubatch has its own device buffers, and the step ends when the last download has
+        landed (the compute stream waits for the download stream)."""
         t = self.torch
+        cur = t.cuda.current_stream()
+        if not hasattr(self, "_e2e_streams"):
+            self._e2e_streams = (t.cuda.Stream(), t.cuda.Stream())
+            n = len(self.ub)
+            self._e2e_in = [t.cuda.Event() for _ in range(n)]
+            self._e2e_done = [t.cuda.Event() for _ in range(n)]
+        up, down = self._e2e_streams
         h2d = d2h = 0
-        for d, h, ho in zip(self.ub, self.host, self.host_out):
-            for k_ in ("tok_seq", "tok_pos", "q", "k", "v"):
-                d[k_].copy_(h[k_], non_blocking=True)
-                h2d += h[k_].numel() * h[k_].element_size()
+        up.wait_stream(cur)
+        with t.cuda.stream(up):
+            for d, h, ev in zip(self.ub, self.host, self._e2e_in):
+                for k_ in ("tok_seq", "tok_pos", "q", "k", "v"):
+                    d[k_].copy_(h[k_], non_blocking=True)
+                    h2d += h[k_].numel() * h[k_].element_size()
+                ev.record(up)
+        down.wait_stream(cur)
+        for d, ev_in, ev_done in zip(self.ub, self._e2e_in, self._e2e_done):
+            cur.wait_event(ev_in)
             self._ubatch(d)
-            ho.copy_(d["out"], non_blocking=True)
-            d2h += ho.numel() * ho.element_size()
+            ev_done.record(cur)
+        with t.cuda.stream(down):
+            for d, ho, ev in zip(self.ub, self.host_out, self._e2e_done):
+                down.wait_event(ev)
+                ho.copy_(d["out"], non_blocking=True)
+                d2h += ho.numel() * ho.element_size()
+        cur.wait_stream(down)
         return h2d, d2h
 
 
