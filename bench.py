@@ -41,9 +41,9 @@ METRIC = "decode KV GB/s + prefill TFLOP/s, Qwen3-8B-shape paged attn, 8×16K, 1
 # commands: profiles/.
 TRAFFIC = {
     "k_prefill": {"bytes": 668.2e6, "files": ["k_prefill.cu"], "digest": "e959f50d1158df2f"},
-    "k_decode": {"bytes": 86.12e6, "files": ["k_decode.cu"], "digest": "c41185ea7d688a2b"},
-    "k_decode_span": {"bytes": 116.23e6, "files": ["k_decode.cu"], "digest": "c41185ea7d688a2b"},
-    "k_decode_fp8": {"bytes": 43.67e6, "files": ["k_decode.cu"], "digest": "c41185ea7d688a2b"},
+    "k_decode": {"bytes": 86.20e6, "files": ["k_decode.cu"], "digest": "96c5b32d878880b2"},
+    "k_decode_span": {"bytes": 116.61e6, "files": ["k_decode.cu"], "digest": "96c5b32d878880b2"},
+    "k_decode_fp8": {"bytes": 43.67e6, "files": ["k_decode.cu"], "digest": "96c5b32d878880b2"},
     "k_copy_pages": {"bytes": 488.08e6, "files": ["k_small.cu"], "digest": "7c947439bca9c5a5"},
 }
 _TRAFFIC_HEADERS = ["common.cuh", "tc.cuh", "tmap.cuh", "kernels.cuh"]

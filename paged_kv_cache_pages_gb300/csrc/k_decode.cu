@@ -304,6 +304,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
   using Cfg = DecCfg<D, G, MASK, KV8>;
   constexpr int NS = Cfg::NS;
+  // units asked of L2 before the dependency wait, so that the first blocks stream in
+  // while the launch before drains (the depth of each variant is the measured best)
+  constexpr int kPre = KV8 ? 6 : MASK ? 3 : 6;
   constexpr int KSTEPS = D / 16;  // k-steps of the QK contraction
   constexpr int NT = D / 8;       // 8-dim tiles of the PV product
   static_assert(G <= 8, "the group fits in rows 0..7 of the 16-row tile");
@@ -349,31 +352,54 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
     const int4 *srec = reinterpret_cast<const int4 *>(a.ws + a.lay.dec_start) + 4 * blockIdx.x;
     const int4 s0 = __ldcg(srec), s1 = __ldcg(srec + 1), p0 = __ldcg(srec + 2),
                p1 = __ldcg(srec + 3);
+    const int2 cnt0 =
+        KV8 ? make_int2(0, 0) : ld_v2_early(&reinterpret_cast<const WsHeader *>(a.ws)->n_dec);
     const int g = s0.y, kb = s0.z, tok = s0.w, units = s1.x;
     const int ppb = KB / a.P;  // pages per key block
+    // the length of the CTA's range, as the plan cuts it
+    const int U0 = cnt0.y, C0 = min((int)gridDim.x, U0);
+    const int n0 = (int)blockIdx.x < C0 ? (int)((int64_t)(blockIdx.x + 1) * U0 / C0 -
+                                               (int64_t)blockIdx.x * U0 / C0)
+                                        : 0;
     // a CTA without units has no record: only in-range rows are looked up
-    const bool sane = tok >= 0 && tok < a.T && kb >= 0 && g >= 0 && g < a.Hkv;
-    // the page ids of the next units, all requested before the first is used
-    // (single-page blocks, the usual case; wider blocks prefetch their first unit only)
-    const int nu = !sane ? 0 : ppb == 1 ? min(min(NS, units - kb), a.max_pages - kb) : 1;
-    int pid[6];
+    const bool sane = tok >= 0 && tok < a.T && kb >= 0 && g >= 0 && g < a.Hkv && units > 0 &&
+                      kb < units;
+    // The first kPre units of the range, continuing into the token's next heads (which
+    // use the same page ids; FP8 pages: the first head's units only); all page ids are
+    // requested as soon as the record is in, before the first is used, and the range
+    // length bounds only the prefetches.  Single-page blocks, the usual case; wider
+    // blocks prefetch their first unit only.
+    const int nld = !sane ? 0 : ppb != 1 ? 1 : KV8 ? min(kPre, units - kb) : kPre;
+    int pid[kPre], gid[kPre];
+    int ku = kb, gu = sane ? g : a.Hkv;  // (block, head) of unit u, stepped without division
 #pragma unroll
-    for (int u = 0; u < 6; ++u) {
-      const int32_t *row = a.tpt + (size_t)tok * a.max_pages + (size_t)(kb + u);
-      pid[u] = u == 0 ? p0.x : (u < nu ? __ldcg(row) : -1);
+    for (int u = 0; u < kPre; ++u) {
+      gid[u] = gu;
+      pid[u] = u == 0 ? p0.x
+                      : (u < nld && gu < a.Hkv ? __ldcg(a.tpt + (size_t)tok * a.max_pages + ku) : -1);
+      if (++ku >= units) {
+        ku = 0;
+        ++gu;
+      }
     }
+    const int nu = KV8 ? nld : min(nld, n0);
     const int pg0[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
     for (int u = 0; u < nu; ++u) {
+      int pu = pid[0], gu = gid[0];
+#pragma unroll
+      for (int x = 1; x < kPre; ++x)
+        if (u == x) {
+          pu = pid[x];
+          gu = gid[x];
+        }
+      if (gu >= a.Hkv) break;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         if (j >= ppb) break;
-        int page = pg0[j];
-#pragma unroll
-        for (int x = 1; x < 6; ++x)
-          if (u == x) page = pid[x];
+        const int page = ppb == 1 ? pu : pg0[j];
         if (page < 0 || page >= a.num_pages) continue;
-        const int y = (page * a.Hkv + g) * a.P;
-        const int yv = KV8 ? (page * a.Hkv + g) * D : y;  // FP8 V: [page][h][d][P]
+        const int y = (page * a.Hkv + gu) * a.P;
+        const int yv = KV8 ? (page * a.Hkv + gu) * D : y;  // FP8 V: [page][h][d][P]
         for (int hf = 0; hf < Cfg::kHalves; ++hf) {
           tc::tma_prefetch_2d(&maps.k, hf * 64, y);
           tc::tma_prefetch_2d(&maps.v, hf * 64, yv);
