@@ -407,6 +407,26 @@ def cpu_baseline_prefill(wl, budget_s=12.0):
                       f"prefill, all 32 heads, fp64; {secs:.1f} s of CPU work"}
 
 
+def cpu_baseline_decode(case, reps_budget_s=3.0):
+    """The oracle as it stands on host cores, on the whole decode layer (all 8 tokens,
+    all heads): KV bytes the layer reads per second of oracle time."""
+    import oracle
+    tpt, kv, slot = oracle.expand_ubatch(case.seq_page_table(), case.tok_seq, case.tok_pos, case.P)
+    kp, vp = case.k_pool.copy(), case.v_pool.copy()
+    oracle.kv_append(case.k_new, case.v_new, slot, kp, vp)
+    nbytes = float(kv.astype(np.int64).sum()) * case.Hkv * case.d * 2 * 2
+    secs, reps = 0.0, 0
+    while secs < reps_budget_s:
+        t0 = time.perf_counter()
+        oracle.paged_attention(case.q, kp, vp, tpt, kv, case.scale)
+        secs += time.perf_counter() - t0
+        reps += 1
+    return {"value": round(nbytes * reps / secs / 1e9, 3), "unit": "GB/s",
+            "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"the whole decode layer (8 tokens, 32 heads, fp64), {reps} runs in "
+                      f"{secs:.1f} s"}
+
+
 # ----------------------------------------------------------------------------- arms
 
 def bench_copy_pages(pa, torch, dev, steps, warmup, world, hbm, with_cpu, seed=0):
@@ -651,6 +671,7 @@ def run_ours(args):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_prefill(pb.wl, budget_s=args.cpu_budget)
+        line["decode"]["cpu_baseline"] = cpu_baseline_decode(db.case)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
