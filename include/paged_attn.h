@@ -50,6 +50,9 @@
  *    kv_len beyond the row's capacity, a bounded wait that timed out) never
  *    trap: the kernel skips the bad access, records a PA_ERR_* bit in the
  *    workspace error word, and paged_attn_read_error returns it.
+ *  - Tracing: every call that launches kernels opens an NVTX range named after
+ *    itself for its duration on the host, so a profiler's timeline shows which
+ *    call launched which kernels.  Without a tool attached it costs nothing.
  */
 #ifndef PAGED_ATTN_H
 #define PAGED_ATTN_H
