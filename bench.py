@@ -52,7 +52,9 @@ _TRAFFIC_HEADERS = ["common.cuh", "tc.cuh", "tmap.cuh", "kernels.cuh"]
 def traffic_of(kernel: str):
     """Recorded DRAM bytes per launch of `kernel`, or None if its sources changed."""
     import hashlib
-    rec = TRAFFIC[kernel]
+    rec = TRAFFIC.get(kernel)
+    if rec is None:
+        return None
     csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "paged_kv_cache_pages_gb300",
                         "csrc")
     h = hashlib.sha256()
@@ -158,6 +160,58 @@ def aggregate(units_per_rank: float, seconds_max: float, world: int) -> float:
     return units_per_rank * world / seconds_max
 
 
+def measure_f16_peak(torch, dev, gpu_index, n=8192, sustain_s=4.0):
+    """Dense f16 tensor peak on this GPU, measured like the bf16 entries of the peak
+    file: torch.matmul of two n x n f16 matrices (2 n^3 FLOP), best of 10 launches
+    timed by CUDA events (burst), and launches back to back for sustain_s seconds
+    (sustained, under the power cap), with the SM clocks sampled during each."""
+    a = torch.randn(n, n, dtype=torch.float16, device=dev)
+    b = torch.randn(n, n, dtype=torch.float16, device=dev)
+    c = torch.empty(n, n, dtype=torch.float16, device=dev)
+    flop = 2.0 * n ** 3
+    for _ in range(5):
+        torch.matmul(a, b, out=c)
+    torch.cuda.synchronize()
+    best = float("inf")
+    with ClockSampler(gpu_index) as clk_b:
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch.matmul(a, b, out=c)
+            e1.record()
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1) / 1e3)
+    with ClockSampler(gpu_index) as clk_s:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        count = 0
+        t_end = time.perf_counter() + sustain_s
+        e0.record()
+        while time.perf_counter() < t_end:
+            for _ in range(16):
+                torch.matmul(a, b, out=c)
+            count += 16
+            torch.cuda.synchronize()
+        e1.record()
+        torch.cuda.synchronize()
+        sus = e0.elapsed_time(e1) / 1e3
+    del a, b, c
+    return {"burst": round(flop / best / 1e12, 1), "sustained": round(flop * count / sus / 1e12, 1),
+            "burst_clocks": clk_b.summary(), "sustained_clocks": clk_s.summary(),
+            "how": f"torch.matmul f16 {n}^3: best of 10 (burst); back to back for "
+                   f"{sustain_s:.0f} s (sustained)"}
+
+
+def clock_matched_peak(clocks, burst, sustained):
+    """The peak that a kernel timed under `clocks` can earn: the burst figure when its
+    median SM clock sat at the maximum with no power cap, else the sustained one."""
+    mhz, top = clocks.get("sm_mhz"), clocks.get("sm_max_mhz")
+    at_max = bool(mhz and top and mhz >= 0.97 * top)
+    capped = "sw_power_cap" in (clocks.get("reasons") or [])
+    if at_max and not capped:
+        return burst, "burst (kernel clocks at maximum, no power cap)"
+    return sustained, "sustained (kernel clocks below maximum or power-capped)"
+
+
 # ----------------------------------------------------------------------------- prefill leg
 
 class PrefillBench:
@@ -251,10 +305,10 @@ class PrefillBench:
 # ----------------------------------------------------------------------------- decode leg
 
 class DecodeBench:
-    def __init__(self, pa, torch, dev, seed=0, layers=DECODE_LAYERS):
+    def __init__(self, pa, torch, dev, seed=0, layers=DECODE_LAYERS, case=None):
         import workloads
         self.pa, self.torch = pa, torch
-        self.case = c = workloads.decode(seed)
+        self.case = c = workloads.decode(seed) if case is None else case
         t = torch
         self.spt = t.from_numpy(c.seq_page_table()).to(dev)
         self.tok_seq = t.from_numpy(c.tok_seq).to(dev)
@@ -379,9 +433,11 @@ def capture_step(torch, fn):
     return g
 
 
-def cpu_baseline_prefill(wl, budget_s=12.0):
+def cpu_baseline_prefill(wl, budget_s=12.0, keep=False):
     """The oracle as it stands on host cores: sampled tokens of the middle
-    ubatches of the 8x16K prefill, growing the sample until ~budget_s of work."""
+    ubatches of the 8x16K prefill, growing the sample until ~budget_s of work.
+    keep=True also returns the oracle's outputs [(ubatch, tokens, out)], which the
+    benchmark compares with the GPU outputs of the same ubatches."""
     import oracle
     kp, vp = wl.pool_final()
     mids = list(range(len(wl.ubatches) // 2, len(wl.ubatches)))
@@ -390,21 +446,48 @@ def cpu_baseline_prefill(wl, budget_s=12.0):
     n_tok = 0
     stride = 64
     i = 0
+    kept = []
     while secs < budget_s and i < len(mids):
         u = mids[i]
         ts, tp, q, _, _ = wl.ubatch(u)
         tpt, kv, _ = oracle.expand_ubatch(wl.seq_page_table, ts, tp, wl.P)
         sel = np.arange(0, ts.shape[0], stride, dtype=np.int32)
         t0 = time.perf_counter()
-        oracle.paged_attention(q, kp, vp, tpt, kv, wl.scale, tokens=sel)
+        ref = oracle.paged_attention(q, kp, vp, tpt, kv, wl.scale, tokens=sel)
         secs += time.perf_counter() - t0
+        if keep:
+            kept.append((u, sel, ref))
         flops += 4.0 * wl.d * wl.Hq * float(kv[sel].astype(np.int64).sum())
         n_tok += len(sel)
         i += 1
-    return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
-            "kind": "oracle",
-            "sample": f"{n_tok} tokens (every {stride}th) of {i} late ubatches of the 8x16K "
-                      f"prefill, all 32 heads, fp64; {secs:.1f} s of CPU work"}
+    res = {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+           "kind": "oracle",
+           "sample": f"{n_tok} tokens (every {stride}th) of {i} late ubatches of the 8x16K "
+                     f"prefill, all 32 heads, fp64; {secs:.1f} s of CPU work"}
+    return (res, kept) if keep else res
+
+
+ATOL, RTOL = 2e-3, 1e-2   # |gpu - oracle| <= ATOL + RTOL |oracle|, elementwise
+
+
+def parity_check(kept, gpu_rows):
+    """Element-wise comparison of GPU outputs with the oracle's on the sampled
+    tokens.  gpu_rows(u, tokens) -> float array [n][Hq][d].  Returns a record; the
+    benchmark refuses to print a number whose check failed."""
+    n_tok = n_bad = 0
+    max_abs = 0.0
+    finite = True
+    for u, sel, ref in kept:
+        got = np.asarray(gpu_rows(u, sel), np.float64)
+        finite &= bool(np.all(np.isfinite(got)))
+        err = np.abs(got - ref)
+        n_bad += int((err > ATOL + RTOL * np.abs(ref)).sum())
+        max_abs = max(max_abs, float(np.nanmax(err)) if err.size else 0.0)
+        n_tok += len(sel)
+    return {"tokens": n_tok, "ubatches": len(kept), "max_abs": max_abs,
+            "out_of_tolerance": n_bad, "finite": finite,
+            "ok": bool(finite and n_bad == 0 and n_tok > 0),
+            "tolerance": f"|gpu - oracle| <= {ATOL} + {RTOL} |oracle| elementwise"}
 
 
 def cpu_baseline_decode(case, reps_budget_s=3.0):
@@ -562,6 +645,149 @@ def bench_fp8_decode(pa, torch, db, steps, warmup, world, hbm, f16_ms_per_layer)
             "timing": "CUDA graph of one plan and 36 FP8 decode launches (one per layer)"}
 
 
+LONGTAIL_LAYERS = 4
+
+
+def bench_longtail(pa, torch, dev, steps, warmup, world, hbm, with_cpu, seed=0):
+    """Long-tail decode: 64 sequences, KV lengths lognormal (median 2048, clipped to
+    256..32768), 30% free pages; about 0.85 GB of K/V per layer, so 4 layers over 4
+    distinct pools exceed L2 many times over.  One expansion and plan, then per layer
+    append + decode (the split-KV path with its fused reduce)."""
+    import workloads
+    db = DecodeBench(pa, torch, dev, seed=seed, layers=LONGTAIL_LAYERS,
+                     case=workloads.longtail(seed))
+    g = capture_step(torch, db.step)
+    total, _ = time_steps(torch, g.replay, steps, warmup, world)
+    a_graph = capture_step(torch, db.attention_only)
+    kern, _ = time_steps(torch, a_graph.replay, steps, warmup, world)
+    if pa.read_error(db.ws):
+        raise RuntimeError("device error word set in the long-tail decode")
+    t_step = max_over_ranks(total / 1e3 / steps, world)
+    t_kern = kern / 1e3 / (steps * db.layers)
+    ach = db.bytes_per_layer / t_kern / 1e9
+    c = db.case
+    res = {"workload": "decode_longtail_64seq", "unit": "GB/s",
+           "value": round(aggregate(db.bytes_per_layer * db.layers, t_step, world) / 1e9, 1),
+           "layers": db.layers, "kv_bytes_per_layer": db.bytes_per_layer,
+           "ms_per_step": round(t_step * 1e3, 4), "ms_per_layer_decode": round(t_kern * 1e3, 4),
+           "seq_len": {"min": int(c.seq_len.min()), "median": float(np.median(c.seq_len)),
+                       "max": int(c.seq_len.max())},
+           "gpu_launches": db.launches_per_step * steps,
+           "roofline": {"bound": "hbm", "kernel": "k_decode", "achieved": round(ach, 1),
+                        "peak": hbm, "unit": "GB/s", "frac": round(ach / hbm, 4),
+                        "timing": "CUDA events around a graph of the 4 decode launches back to "
+                                  "back (appends left out)",
+                        "traffic": traffic_of("k_decode_longtail")},
+           "timing": "value: CUDA graph of expansion, plan and 4 x (append + decode)"}
+    if with_cpu:
+        res["cpu_baseline"] = cpu_baseline_decode(c, reps_budget_s=3.0)
+        res["cpu_baseline"]["sample"] = res["cpu_baseline"]["sample"].replace(
+            "8 tokens", f"{c.T} tokens")
+    return res
+
+
+MIXED_LAYERS = 8
+
+
+def mixed_unique_bytes(case):
+    """K/V bytes of the distinct (page, KV head) blocks a ubatch reads, each counted
+    once, only the rows below each reader's kv_len (the shared prefix counts once),
+    against the logical bytes (every token's own sequence K/V)."""
+    P, row = case.P, case.Hkv * case.d * 2 * 2     # K + V bytes of one cached row
+    rows_of_page = {}
+    logical = 0
+    for s, p in zip(case.tok_seq, case.tok_pos):
+        if s < 0:
+            continue
+        L = int(p) + 1
+        logical += L * row
+        pages = case.seq_pages[int(s)]
+        for j in range(-(-L // P)):
+            pg = int(pages[j])
+            rows_of_page[pg] = max(rows_of_page.get(pg, 0), min(P, L - j * P))
+    return float(sum(rows_of_page.values()) * row), float(logical)
+
+
+def bench_mixed(pa, torch, dev, steps, warmup, world, hbm, tensor_peak, with_cpu, seed=0):
+    """The shared-prefix mixed ubatch: 16 sequences share 64 prefix pages (8192 tokens);
+    12 decode tokens plus 4 x 256 prefill tokens in one ubatch.  One expansion and
+    plan (prefill tiles and decode items in the same plan), then per layer append +
+    run (the tcgen05 prefill launch, then the split-KV decode launch), over 8 distinct
+    pools.  Roofline: the time the ubatch needs at least, max(unique K/V bytes / HBM
+    peak, FLOPs / tensor peak), over the measured time."""
+    import workloads
+    c = workloads.shared_prefix(seed)
+    t = torch
+    spt = t.from_numpy(c.seq_page_table()).to(dev)
+    ts, tp = t.from_numpy(c.tok_seq).to(dev), t.from_numpy(c.tok_pos).to(dev)
+    kp = t.from_numpy(c.k_pool.view(np.float16)).to(dev)
+    vp = t.from_numpy(c.v_pool.view(np.float16)).to(dev)
+    pools = [(kp.clone(), vp.clone()) for _ in range(MIXED_LAYERS)]
+    qs = [t.from_numpy(c.q.view(np.float16)).to(dev) for _ in range(MIXED_LAYERS)]
+    kn, vn = t.from_numpy(c.k_new.view(np.float16)).to(dev), t.from_numpy(c.v_new.view(np.float16)).to(dev)
+    outs = [t.empty_like(qs[0]) for _ in range(MIXED_LAYERS)]
+    ws = pa.new_workspace(c.T, c.Hq, c.Hkv, c.d, dev)
+    tpt = t.empty((c.T, c.max_pages), dtype=t.int32, device=dev)
+    kv = t.empty(c.T, dtype=t.int32, device=dev)
+    slot = t.empty(c.T, dtype=t.int64, device=dev)
+
+    def step():
+        pa.expand_ubatch(spt, ts, tp, c.P, out=(tpt, kv, slot))
+        pa.plan(tpt, kv, c.Hq, c.Hkv, c.P, c.d, ws)
+        for l in range(MIXED_LAYERS):
+            pa.kv_append(kn, vn, slot, *pools[l])
+            pa.run(qs[l], *pools[l], tpt, kv, c.scale, outs[l], ws)
+
+    g = capture_step(torch, step)
+    total, _ = time_steps(torch, g.replay, steps, warmup, world)
+    if pa.read_error(ws):
+        raise RuntimeError("device error word set in the mixed shared-prefix ubatch")
+    t_step = max_over_ranks(total / 1e3 / steps, world)
+    t_layer = t_step / MIXED_LAYERS
+    kv_len = c.tok_pos.astype(np.int64) + 1
+    flops = 4.0 * c.d * c.Hq * float(kv_len.sum())
+    uniq, logical = mixed_unique_bytes(c)
+    t_min = max(uniq / (hbm * 1e9), flops / (tensor_peak * 1e12))
+    res = {"workload": "mixed_shared_prefix_12dec_1024pf", "unit": "TFLOP/s",
+           "value": round(aggregate(flops * MIXED_LAYERS, t_step, world) / 1e12, 2),
+           "layers": MIXED_LAYERS, "ms_per_layer": round(t_layer * 1e3, 4),
+           "flops_per_layer": flops, "unique_kv_bytes_per_layer": uniq,
+           "logical_kv_bytes_per_layer": logical,
+           "unique_gbs": round(uniq / t_layer / 1e9, 1),
+           "logical_gbs": round(logical / t_layer / 1e9, 1),
+           "roofline": {"bound": "tensor" if flops / (tensor_peak * 1e12) >= uniq / (hbm * 1e9)
+                        else "hbm",
+                        "kernel": "k_prefill + k_decode (one layer of the ubatch)",
+                        "achieved": round(flops / t_layer / 1e12, 2), "peak": tensor_peak,
+                        "unit": "TFLOP/s", "frac": round(t_min / t_layer, 4),
+                        "hbm_peak_gbs": hbm, "t_min_ms": round(t_min * 1e3, 4),
+                        "note": "frac = max(unique bytes / HBM peak, FLOPs / tensor peak) "
+                                "/ measured time per layer (append, prefill and decode launches)",
+                        "traffic": None},
+           "gpu_launches": (2 + 3 * MIXED_LAYERS + 1) * steps,
+           "timing": "CUDA graph of expansion, plan and 8 x (append + prefill + decode)"}
+    if with_cpu:
+        import oracle
+        tpt_h, kv_h, slot_h = oracle.expand_ubatch(c.seq_page_table(), c.tok_seq, c.tok_pos, c.P)
+        kph, vph = c.k_pool.copy(), c.v_pool.copy()
+        oracle.kv_append(c.k_new, c.v_new, slot_h, kph, vph)
+        sel = np.concatenate([np.arange(12), np.arange(12, c.T, 16)]).astype(np.int32)
+        t0 = time.perf_counter()
+        ref = oracle.paged_attention(c.q, kph, vph, tpt_h, kv_h, c.scale, tokens=sel)
+        secs = time.perf_counter() - t0
+        f_s = 4.0 * c.d * c.Hq * float(kv_h[sel].astype(np.int64).sum())
+        res["cpu_baseline"] = {"value": f_s / secs / 1e12, "unit": "TFLOP/s",
+                               "cores": oracle.num_threads(), "kind": "oracle",
+                               "sample": f"the 12 decode tokens and every 16th prefill token "
+                                         f"({len(sel)} tokens, all heads, fp64), {secs:.1f} s"}
+        res["parity"] = parity_check(
+            [(0, sel, ref)],
+            lambda u, s_: outs[-1][t.from_numpy(s_).long().to(dev)].float().cpu().numpy())
+        if not res["parity"]["ok"]:
+            raise RuntimeError(f"mixed ubatch outputs differ from the oracle: {res['parity']}")
+    return res
+
+
 def run_ours(args):
     import torch
     world, rank, local = dist_setup()
@@ -592,7 +818,8 @@ def run_ours(args):
     value = aggregate(pb.flops, t_step, world) / 1e12
     t_kern = kern_ms / 1e3 / (args.steps * n_ub)             # average prefill launch
     achieved = pb.flops / n_ub / t_kern / 1e12
-    peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    f16 = measure_f16_peak(torch, dev, local)
+    peak, peak_how = clock_matched_peak(clocks, f16["burst"], f16["sustained"])
 
     # end to end: pinned host buffers, copies inside the timed region
     for _ in range(args.warmup):
@@ -638,7 +865,15 @@ def run_ours(args):
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "tensor", "kernel": "k_prefill", "achieved": round(achieved, 2),
                      "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                     "peak_source": f"{peak_src} bf16 sustained (f16 dense rate = bf16)",
+                     "peak_source": f"measured in this run: f16 {peak_how}",
+                     "peak_f16_burst": f16["burst"], "peak_f16_sustained": f16["sustained"],
+                     "frac_vs_f16_burst": round(achieved / f16["burst"], 4),
+                     "frac_vs_f16_sustained": round(achieved / f16["sustained"], 4),
+                     "f16_peak": f16,
+                     "peak_file_bf16": {"burst": peaks.get("bf16_tflops"),
+                                        "sustained": peaks.get("bf16_tflops_sustained"),
+                                        "source": peak_src},
+                     "per_step_frac": round(value / world / peak, 4),
                      "traffic": traffic_of("k_prefill")},
         "e2e": {"value": round(aggregate(pb.flops, e2e_s, world) / 1e12, 3), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -669,9 +904,24 @@ def run_ours(args):
         "fp8_pages": bench_fp8_decode(pa, torch, db, args.steps, args.warmup, world, hbm,
                                       d_kt * 1e3),
     }
+    line["longtail"] = bench_longtail(pa, torch, dev, args.steps, args.warmup, world, hbm,
+                                      with_cpu=rank == 0 and world == 1 and not args.no_cpu_baseline,
+                                      seed=args.seed)
+    line["mixed_shared_prefix"] = bench_mixed(
+        pa, torch, dev, args.steps, args.warmup, world, hbm, peak,
+        with_cpu=rank == 0 and world == 1 and not args.no_cpu_baseline, seed=args.seed)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline_prefill(pb.wl, budget_s=args.cpu_budget)
+        line["cpu_baseline"], kept = cpu_baseline_prefill(pb.wl, budget_s=args.cpu_budget,
+                                                          keep=True)
         line["decode"]["cpu_baseline"] = cpu_baseline_decode(db.case)
+        # the outputs the timed steps left in each ubatch's buffer, against the oracle
+        line["parity"] = parity_check(
+            kept, lambda u, sel: pb.ub[u]["out"][torch.from_numpy(sel).long().to(dev)]
+            .float().cpu().numpy())
+        if not line["parity"]["ok"]:
+            raise RuntimeError(f"8x16K outputs differ from the oracle: {line['parity']}")
+    else:
+        line["parity"] = None
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

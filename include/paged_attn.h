@@ -200,7 +200,10 @@ int paged_attn_forward(const uint16_t *q, const uint16_t *k_pages, const uint16_
  * address; make that first call before any stream capture.  Every call shares
  * the array and it keeps the last call's contents (each call clears what it
  * needs); calls that overlap on the GPU race and must be serialised.  The
- * device error word of these calls is not exposed.
+ * device error word of these calls is not exposed, so a bad page id or kv_len
+ * goes unreported (the bad access is still skipped, never made): check the
+ * tables with paged_attn_validate first.  Every input gets the status that
+ * paged_attn_forward would return for it (the same checks, in the same order).
  */
 int paged_attn_forward_noalloc(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
                                const int32_t *tok_page_table, int max_pages,

@@ -53,13 +53,18 @@ extern "C" int paged_attn_forward_noalloc(const uint16_t *q, const uint16_t *k_p
                                           int max_pages, const int32_t *tok_kv_len, int T, int Hq,
                                           int Hkv, int P, int d, int num_pages, float scale,
                                           uint16_t *out, void *stream) {
-  if (T < 0) return PA_EINVAL;
-  if (T == 0) return PA_OK;
+  // The argument and shape checks of paged_attn_forward, in its order: with no
+  // workspace it returns their first failure, PA_OK for an empty ubatch, or
+  // PA_EWORKSPACE once everything but the workspace is acceptable.  So every input
+  // gets the same status from both calls.
+  int st = paged_attn_forward(q, k_pages, v_pages, tok_page_table, max_pages, tok_kv_len, T, Hq,
+                              Hkv, P, d, num_pages, scale, out, nullptr, 0, stream);
+  if (st != PA_EWORKSPACE) return st;
   const size_t need = paged_attn_workspace_size(T, Hq, Hkv, d);
   if (need == 0) return PA_EUNSUPPORTED;
   if (need > kNoAllocScratchBytes) return PA_EWORKSPACE;  // ubatch too large for the fixed scratch
   void *scratch = nullptr;
-  int st = scratch_for_current_device(&scratch);
+  st = scratch_for_current_device(&scratch);
   if (st != PA_OK) return st;
   return paged_attn_forward(q, k_pages, v_pages, tok_page_table, max_pages, tok_kv_len, T, Hq, Hkv,
                             P, d, num_pages, scale, out, scratch, kNoAllocScratchBytes, stream);

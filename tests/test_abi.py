@@ -111,3 +111,30 @@ def test_page_pool(pa):
     with pytest.raises(pa.PagedAttnError):
         pool.share([7])
     assert pool.refcount(99) == pa.PA_EINVAL
+
+
+def test_noalloc_host_checks_match_forward(pa):
+    """The no-allocation entry point returns, for every input its host checks
+    reject, the status paged_attn_forward returns for the same input."""
+    L = pa.lib()
+    fwd, noa = L.paged_attn_forward, L.paged_attn_forward_noalloc
+    noa.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int, ctypes.c_void_p] + [ctypes.c_int] * 6 + \
+        [ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p]
+    noa.restype = ctypes.c_int
+    nul = None
+    # (max_pages, T, Hq, Hkv, P, d, num_pages)
+    cases = [(4, 8, 0, 2, 16, 64, 32),      # Hq <= 0
+             (4, 8, 4, 0, 16, 64, 32),      # Hkv <= 0
+             (4, 8, 4, 2, 16, 80, 32),      # unsupported d
+             (4, 8, 4, 2, 24, 64, 32),      # unsupported P
+             (4, 8, 6, 4, 16, 64, 32),      # Hq % Hkv != 0
+             (4, -1, 4, 2, 16, 64, 32),     # T < 0
+             (4, 0, 4, 2, 16, 80, 32),      # T == 0 with a bad shape
+             (4, 0, 4, 0, 16, 64, 32),      # T == 0 with Hkv == 0
+             (4, 0, 4, 2, 16, 64, 32),      # T == 0, good shape: a no-op
+             (4, 8, 4, 2, 16, 64, 32),      # null tables
+             (0, 8, 4, 2, 16, 64, 32)]      # max_pages == 0
+    for mp, T, Hq, Hkv, P, d, npg in cases:
+        want = fwd(nul, nul, nul, nul, mp, nul, T, Hq, Hkv, P, d, npg, 0.1, nul, nul, 0, nul)
+        got = noa(nul, nul, nul, nul, mp, nul, T, Hq, Hkv, P, d, npg, 0.1, nul, nul)
+        assert got == want, ((mp, T, Hq, Hkv, P, d, npg), got, want)

@@ -3,9 +3,11 @@
 paged_attn_forward_noalloc serves callers that cannot allocate device memory
 (a host framework owning all device memory, a fixed memory budget, or a
 latency-critical path).  It must give the same output as paged_attn_forward
-with an allocated workspace, on two calls in a row (the second call finds the
-first call's leftovers in the shared scratch), and reject a ubatch too large
-for its fixed 64 MiB scratch.  This file is collected last on purpose.
+with an allocated workspace, and match the fp64 oracle, on two calls in a row
+(the second call finds the first call's leftovers in the shared scratch); a
+call with a bad page id must stay harmless (the bad access is skipped) and leave
+the next call correct; and a ubatch too large for its fixed 64 MiB scratch is
+rejected.  This file is collected last on purpose.
 """
 import ctypes
 
@@ -15,7 +17,7 @@ import pytest
 torch = pytest.importorskip("torch")
 
 import workloads
-from tests._gpu import GpuCase, assert_attn_close
+from tests._gpu import GpuCase, assert_attn_close, oracle_case
 
 pytestmark = pytest.mark.gpu
 
@@ -28,10 +30,11 @@ def _noalloc(lib):
     return fn
 
 
-def _call(fn, g, out):
+def _call(fn, g, out, tpt=None):
     c = g.case
+    tpt = g.tpt if tpt is None else tpt
     p = lambda t: ctypes.c_void_p(t.data_ptr())
-    return fn(p(g.q), p(g.kp), p(g.vp), p(g.tpt), g.tpt.shape[1], p(g.kv), c.T, c.Hq, c.Hkv, c.P,
+    return fn(p(g.q), p(g.kp), p(g.vp), p(tpt), tpt.shape[1], p(g.kv), c.T, c.Hq, c.Hkv, c.P,
               c.d, c.num_pages, c.scale, p(out),
               ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
 
@@ -48,7 +51,27 @@ def test_noalloc_matches_forward_on_two_calls_in_a_row():
         out = torch.full_like(g.q, float("nan"))
         assert _call(fn, g, out) == pa.PA_OK
         torch.cuda.synchronize()
-        assert_attn_close(out.float().cpu().numpy(), ref, f"noalloc {case.name}")
+        got = out.float().cpu().numpy()
+        assert_attn_close(got, ref, f"noalloc {case.name} vs forward")
+        assert_attn_close(got, oracle_case(case)[0], f"noalloc {case.name} vs oracle")
+
+
+def test_noalloc_bad_page_id_is_harmless_and_next_call_is_correct():
+    import paged_kv_cache_pages_gb300 as pa
+    fn = _noalloc(pa.lib())
+    case = workloads.small_prefill(22, P=16, d=64, Hq=4, Hkv=2)
+    g = GpuCase(pa, case)
+    torch.cuda.synchronize()
+    bad = g.tpt.clone()
+    bad[0, 0] = case.num_pages + 5
+    out = torch.zeros_like(g.q)
+    assert _call(fn, g, out, tpt=bad) == pa.PA_OK    # host checks pass; the access is skipped
+    torch.cuda.synchronize()
+    out = torch.full_like(g.q, float("nan"))
+    assert _call(fn, g, out) == pa.PA_OK
+    torch.cuda.synchronize()
+    assert_attn_close(out.float().cpu().numpy(), g.forward(pa).float().cpu().numpy(),
+                      "noalloc after a bad call")
 
 
 def test_noalloc_rejects_ubatch_beyond_its_scratch():
