@@ -22,7 +22,8 @@ namespace pa {
 //   tile_off       int  [T + 1]  prefix sums of prefill work (key blocks x items) per tile
 //   dec_start      int4 [4C]     first decode unit of each CTA: (i, g, kb, token), (units, kv_len, first block of i, -),
 //                                  then the page ids of that unit's key block (8 ints, -1 past its end)
-//   pf_start       int4 [C]      first prefill unit of each CTA: (tile, item in tile, kb, -)
+//   pf_start       int4 [C]      first prefill unit of each CTA: (tile, item in tile, kb,
+//                                  tile * items per tile + item of the CTA's last unit)
 //   pf_cnt         int  [T * Hkv * NP * 2 * 4]  arrival counters of split prefill items,
 //                                  one per (item, softmax warpgroup, warp)
 //   dec_cnt        int  [T * Hkv]   arrival counters of decode segments split over CTAs
@@ -160,6 +161,11 @@ __device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src_gmem, u
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
       ::"r"(smem_u32(dst_smem)), "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
+}
+
+// Bring `bytes` (a multiple of 16, 16-byte aligned address) of global memory into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ float exp2_approx(float x) {

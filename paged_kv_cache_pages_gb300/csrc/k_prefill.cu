@@ -18,14 +18,20 @@
 //   warp 8     TMA producer: Q tiles (3-D map over [T][Hq][d]) and, for each
 //              128-key block, the K and V boxes of the tile's pages (2-D map
 //              over the pool rows), 128-byte swizzled, 2-stage ring
-//   warp 9     MMA issuer: S_i = Q_i K^T (SS, f16 -> f32 in TMEM), then
-//              O_i += P_i V with P_i read from TMEM (TS), V MN-major in smem
-//   warps 10-11 idle
-// The softmax warpgroups raise their register budget with setmaxnreg (a
-// 128-column score row lives in registers); the third warpgroup lowers its own.
+//   warps 9-10 MMA issuers, one thread each, one per query tile i:
+//              S_i = Q_i K^T (SS, f16 -> f32 in TMEM), then O_i += P_i V with P_i
+//              read from TMEM (TS), V MN-major in smem.  A thread's barrier waits cost
+//              ~100 cycles each even when the phase has completed; with one issuer per
+//              tile, taking turns block by block, the other tile's MMAs keep the tensor
+//              pipe busy meanwhile.
+//   warp 11    idle
+// The softmax warpgroups raise their register budget with setmaxnreg so that a
+// softmax thread holds its whole 128-column score row in registers (one TMEM round
+// trip per block); the third warpgroup lowers its own.
 // TMEM (512 columns): S0 | S1 | O0 | O1.  P_i (f16) overwrites the first 64
-// columns of S_i.  The issue order PV0(kb), S0(kb+1), PV1(kb), S1(kb+1) lets the
-// softmax of one tile run while the tensor core works on the other.
+// columns of S_i.  Tile i's issuer runs PV_i(kb) then S_i(kb+1) (in order on the
+// tensor core, so S_i(kb+1) overwrites P_i only after PV_i read it); the softmax of
+// one tile runs while the tensor core works on the other.
 //
 // Masking: key j of a block is valid for query row t iff j < tok_kv_len[t]
 // (causal per token).  Scores of invalid keys are replaced by -inf (select, so
@@ -39,9 +45,9 @@
 namespace pa {
 
 constexpr int kPfThreads = 384;
-constexpr int kRegsSoftmax = 192;   // per thread, warpgroups 0 and 1
-constexpr int kRegsOther = 120;     // per thread, warpgroup 2
-// registers the split needs from the launch; checked on the host before launching
+constexpr int kRegsSoftmax = 208;   // per thread, warpgroups 0 and 1
+constexpr int kRegsOther = 88;      // per thread, warpgroup 2
+// registers the split needs from the launch (168 x 384); checked on the host before launching
 constexpr int kRegsSplitTotal = 2 * 128 * kRegsSoftmax + 128 * kRegsOther;
 constexpr int kPfStages = 2;
 constexpr int kWarpTma = 8;
@@ -67,6 +73,7 @@ struct PfBars {
   uint64_t q_full, q_empty;
   uint64_t k_full[kPfStages], k_empty[kPfStages], v_full[kPfStages], v_empty[kPfStages];
   uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
+  uint64_t turn[2];  // issuer turns: tile 1's issuer -> tile 0's, tile 0's -> tile 1's
   uint32_t tmem_base;
   int abort;
 };
@@ -88,14 +95,19 @@ __device__ __forceinline__ bool pf_wait(uint64_t *bar, uint32_t parity, int *err
 }
 
 // One contiguous piece of work of a CTA: key blocks [kb_b, kb_e) of one item.
+// A CTA runs its unit range [w0, w1) as [ws, w1) then [w0, ws), ws the first unit of
+// the item holding w1 - 1: the parts of the items it shares with its neighbours then
+// both come early, and so does their combine, instead of at the end of the launch.
 struct Seg {
   int tile, j;              // tile index, item within the tile
   int kb_b, kb_e;           // key-block range of this piece
   int nkb, max_kv;          // whole item: key blocks, longest kv_len of the tile
   int tile_start, n_tok;    // tokens of the tile
   int g, h0, h1;            // KV head, query heads of the pair
-  long long w, w_end;       // unit position of this piece, end of the CTA's range
+  long long w, w_end;       // unit position of this piece, end of the current run
   long long item_start;     // unit index of the item's key block 0
+  int4 rest;                // start (tile, item, kb) of the second run; rest.x < 0: none
+  long long rest_w0, rest_w1;
 };
 
 struct SegCtx {
@@ -117,7 +129,8 @@ __device__ __forceinline__ void seg_load(Seg &s, const SegCtx &x) {
   s.item_start = (long long)x.tile_off[s.tile] + (long long)s.j * s.nkb;
 }
 
-__device__ __forceinline__ bool seg_first(Seg &s, const SegCtx &x, int4 start, long long w0,
+// Start a run of units [w0, w1) at position start = (tile, item, key block).
+__device__ __forceinline__ bool seg_begin(Seg &s, const SegCtx &x, int4 start, long long w0,
                                           long long w1) {
   if (w0 >= w1) return false;
   s.tile = start.x;
@@ -132,7 +145,12 @@ __device__ __forceinline__ bool seg_first(Seg &s, const SegCtx &x, int4 start, l
 
 __device__ __forceinline__ bool seg_next(Seg &s, const SegCtx &x) {
   s.w += s.kb_e - s.kb_b;
-  if (s.w >= s.w_end) return false;
+  if (s.w >= s.w_end) {
+    if (s.rest.x < 0) return false;
+    const int4 r = s.rest;
+    s.rest.x = -1;
+    return seg_begin(s, x, r, s.rest_w0, s.rest_w1);
+  }
   if (++s.j == x.items_per_tile) {  // next tile that has keys (there is one: w < w_end <= W)
     s.j = 0;
     do { ++s.tile; } while (x.tiles[s.tile].z == 0);
@@ -143,12 +161,58 @@ __device__ __forceinline__ bool seg_next(Seg &s, const SegCtx &x) {
   return true;
 }
 
+// The CTA's share of the prefill work, read from the plan.  Each warp role reads it
+// afresh (through an opaque workspace pointer) instead of keeping values from the
+// common prologue live into every role: registers live across the role split must fit
+// the smallest setmaxnreg budget of the roles.
+struct PfWork {
+  SegCtx sx;
+  int4 start;           // first (tile, item, key block) of this CTA
+  long long W, w0, w1;  // total work units; this CTA's range [w0, w1)
+  int C;                // CTAs the plan was cut for
+};
+
+__device__ __forceinline__ PfWork pf_work(const AttnArgs &a, int NP, int G) {
+  uint64_t wsp = reinterpret_cast<uint64_t>(a.ws);
+  asm volatile("" : "+l"(wsp));
+  const unsigned char *ws = reinterpret_cast<const unsigned char *>(wsp);
+  const WsHeader *hdr = reinterpret_cast<const WsHeader *>(ws);
+  PfWork r;
+  r.C = hdr->C;
+  r.W = hdr->pf_work;
+  const int c = blockIdx.x;
+  r.w0 = (long long)c * r.W / r.C;
+  r.w1 = (long long)(c + 1) * r.W / r.C;
+  r.sx.tiles = reinterpret_cast<const int4 *>(ws + a.lay.tiles);
+  r.sx.tile_off = reinterpret_cast<const int *>(ws + a.lay.tile_off);
+  r.sx.Hkv = a.Hkv;
+  r.sx.NP = NP;
+  r.sx.G = G;
+  r.sx.items_per_tile = a.Hkv * NP;
+  r.start = reinterpret_cast<const int4 *>(ws + a.lay.pf_start)[c];
+  return r;
+}
+
+// First piece of the CTA's work (see Seg for the order of its two runs).
+__device__ __forceinline__ bool seg_first(Seg &s, const SegCtx &x, const PfWork &pw) {
+  if (pw.w0 >= pw.w1) return false;
+  const int tl = pw.start.w / x.items_per_tile, jl = pw.start.w - tl * x.items_per_tile;
+  const long long ws = (long long)x.tile_off[tl] + (long long)jl * x.tiles[tl].z;
+  if (ws > pw.w0 && ws < pw.w1) {
+    s.rest = pw.start;
+    s.rest_w0 = pw.w0;
+    s.rest_w1 = ws;
+    return seg_begin(s, x, make_int4(tl, jl, 0, 0), ws, pw.w1);
+  }
+  s.rest.x = -1;
+  return seg_begin(s, x, pw.start, pw.w0, pw.w1);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kPfThreads, 1)
 k_prefill(AttnArgs a, const __grid_constant__ AttnMaps maps) {
   using Cfg = PfCfg<D>;
-  // row record of a split part: O[D] | m | l | pad -- a multiple of 16 bytes so that
-  // every row's record starts 16-byte aligned for float4 access
+  // rows of a split part's record: O[D] | m | l | 2 unused (D + 4 rows of 128 floats)
   constexpr int kPartStride = D + 4;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
@@ -172,26 +236,22 @@ k_prefill(AttnArgs a, const __grid_constant__ AttnMaps maps) {
     for (int x = tid; x < tl.y * a.Hq * (D / 8); x += blockDim.x)
       reinterpret_cast<uint4 *>(a.out + (size_t)tl.x * a.Hq * D)[x] = make_uint4(0, 0, 0, 0);
   }
-  const long long W = hdr->pf_work;
-  const long long w0 = (long long)c * W / C, w1 = (long long)(c + 1) * W / C;
-  if (w0 >= w1) return;
-  SegCtx sx;
-  sx.tiles = tiles;
-  sx.tile_off = reinterpret_cast<const int *>(a.ws + a.lay.tile_off);
-  sx.Hkv = a.Hkv;
-  sx.NP = NP;
-  sx.G = G;
-  sx.items_per_tile = a.Hkv * NP;
-  const int4 start = reinterpret_cast<const int4 *>(a.ws + a.lay.pf_start)[c];
+  {
+    const PfWork pw = pf_work(a, NP, G);
+    if (pw.w0 >= pw.w1) return;
+  }
   if (tid == 0) {
+    // stages and Q tiles are released by both MMA-issuing threads (one per query tile)
     mbar_init(&bars->q_full, 1);
-    mbar_init(&bars->q_empty, 1);
+    mbar_init(&bars->q_empty, NQ);
     for (int s = 0; s < kPfStages; ++s) {
       mbar_init(&bars->k_full[s], 1);
-      mbar_init(&bars->k_empty[s], 1);
+      mbar_init(&bars->k_empty[s], NQ);
       mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->v_empty[s], 1);
+      mbar_init(&bars->v_empty[s], NQ);
     }
+    mbar_init(&bars->turn[0], 1);
+    mbar_init(&bars->turn[1], 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->p_full[i], 128);
@@ -222,13 +282,55 @@ k_prefill(AttnArgs a, const __grid_constant__ AttnMaps maps) {
    if (warp == kWarpTma && lane == 0) {
     // ------------------------------------------------------------ TMA producer
     {
+      const PfWork pw = pf_work(a, NP, G);
+      const SegCtx &sx = pw.sx;
       uint32_t it = 0;
       int nitem = 0;
       const int pages_per_block = KB / a.P;
       const int oob_row = a.num_pages * a.Hkv * a.P;  // first row past the pool: zero fill
-      Seg w;
-      for (bool more = seg_first(w, sx, start, w0, w1); more; more = seg_next(w, sx)) {
-        if (nitem > 0 && !pf_wait(&bars->q_empty, (nitem - 1) & 1, err, abort)) break;
+      Seg w{};
+      const int32_t *row = nullptr;
+      // row coordinate of page j of key block kb in the pool map (past the end when
+      // invalid: the box is zero-filled and nothing outside the pool is touched)
+      auto ycoord = [&](int kb, int j) {
+        int page = row[kb * pages_per_block + j];
+        if (page < 0 || page >= a.num_pages) {
+          atomicOr(err, PA_ERR_PAGE_RANGE);
+          return oob_row;
+        }
+        return (page * a.Hkv + w.g) * a.P;
+      };
+      // K and V boxes of key block kb into ring stage it % kPfStages
+      auto load_kv = [&](int kb) -> bool {
+        const int st = it % kPfStages;
+        const uint32_t ph = (it / kPfStages) & 1u;
+        const int keys = min(KB, w.max_kv - kb * KB);
+        const int npg = (keys + a.P - 1) / a.P;
+        const uint32_t bytes = (uint32_t)npg * a.P * 128u * Cfg::kHalves;
+        if (!pf_wait(&bars->k_empty[st], ph ^ 1u, err, abort)) return false;
+        mbar_arrive_expect_tx(&bars->k_full[st], bytes);
+        for (int j = 0; j < npg; ++j)
+          for (int hf = 0; hf < Cfg::kHalves; ++hf)
+            tc::tma_load_2d(smem + Cfg::kK + st * Cfg::kTile + hf * kBoxBytes + j * a.P * 128,
+                            &maps.k, hf * 64, ycoord(kb, j), &bars->k_full[st]);
+        if (!pf_wait(&bars->v_empty[st], ph ^ 1u, err, abort)) return false;
+        mbar_arrive_expect_tx(&bars->v_full[st], bytes);
+        for (int j = 0; j < npg; ++j)
+          for (int hf = 0; hf < Cfg::kHalves; ++hf)
+            tc::tma_load_2d(smem + Cfg::kV + st * Cfg::kTile + hf * kBoxBytes + j * a.P * 128,
+                            &maps.v, hf * 64, ycoord(kb, j), &bars->v_full[st]);
+        ++it;
+        return true;
+      };
+      for (bool more = seg_first(w, sx, pw); more; more = seg_next(w, sx)) {
+        row = a.tpt + (size_t)w.tile_start * a.max_pages;
+        int kb = w.kb_b;
+        if (nitem > 0) {
+          // the first key block of this item goes into the ring before the Q tiles wait for
+          // the previous item to release them
+          if (!load_kv(kb++)) break;
+          if (!pf_wait(&bars->q_empty, (nitem - 1) & 1, err, abort)) break;
+        }
         mbar_arrive_expect_tx(&bars->q_full, NQ * Cfg::kTile);
         for (int hf = 0; hf < Cfg::kHalves; ++hf) {
           tc::tma_load_3d(smem + Cfg::kQ0 + hf * kBoxBytes, &maps.q, hf * 64, w.h0, w.tile_start,
@@ -237,167 +339,135 @@ k_prefill(AttnArgs a, const __grid_constant__ AttnMaps maps) {
             tc::tma_load_3d(smem + Cfg::kQ1 + hf * kBoxBytes, &maps.q, hf * 64, w.h1,
                             w.tile_start, &bars->q_full);
         }
-        const int32_t *row = a.tpt + (size_t)w.tile_start * a.max_pages;
-        bool ok = true;
-        for (int kb = w.kb_b; kb < w.kb_e && ok; ++kb, ++it) {
-          const int st = it % kPfStages;
-          const uint32_t ph = (it / kPfStages) & 1u;
-          const int keys = min(KB, w.max_kv - kb * KB);
-          const int npg = (keys + a.P - 1) / a.P;
-          const uint32_t bytes = (uint32_t)npg * a.P * 128u * Cfg::kHalves;
-          // row coordinate of page j of this block in the pool map (past the end when invalid:
-          // the box is zero-filled and nothing outside the pool is touched)
-          auto ycoord = [&](int j) {
-            int page = row[kb * pages_per_block + j];
-            if (page < 0 || page >= a.num_pages) {
-              atomicOr(err, PA_ERR_PAGE_RANGE);
-              return oob_row;
+        {  // the next item's Q tiles into L2, so that its load at the switch is short
+          Seg nx = w;
+          if (seg_next(nx, sx))
+            for (int hf = 0; hf < Cfg::kHalves; ++hf) {
+              tc::tma_prefetch_3d(&maps.q, hf * 64, nx.h0, nx.tile_start);
+              if (NQ == 2) tc::tma_prefetch_3d(&maps.q, hf * 64, nx.h1, nx.tile_start);
             }
-            return (page * a.Hkv + w.g) * a.P;
-          };
-          if (!pf_wait(&bars->k_empty[st], ph ^ 1u, err, abort)) { ok = false; break; }
-          mbar_arrive_expect_tx(&bars->k_full[st], bytes);
-          for (int j = 0; j < npg; ++j)
-            for (int hf = 0; hf < Cfg::kHalves; ++hf)
-              tc::tma_load_2d(smem + Cfg::kK + st * Cfg::kTile + hf * kBoxBytes + j * a.P * 128,
-                              &maps.k, hf * 64, ycoord(j), &bars->k_full[st]);
-          if (!pf_wait(&bars->v_empty[st], ph ^ 1u, err, abort)) { ok = false; break; }
-          mbar_arrive_expect_tx(&bars->v_full[st], bytes);
-          for (int j = 0; j < npg; ++j)
-            for (int hf = 0; hf < Cfg::kHalves; ++hf)
-              tc::tma_load_2d(smem + Cfg::kV + st * Cfg::kTile + hf * kBoxBytes + j * a.P * 128,
-                              &maps.v, hf * 64, ycoord(j), &bars->v_full[st]);
         }
+        bool ok = true;
+        for (; kb < w.kb_e && ok; ++kb) ok = load_kv(kb);
         if (!ok) break;
         ++nitem;
       }
     }
-   } else if (warp == kWarpMma) {
-    // ------------------------------------------------------------ MMA issuer
+   } else if ((warp == kWarpMma || warp == kWarpMma + 1) && lane == 0 &&
+              warp - kWarpMma < NQ) {
+    // ------------------------------------------------------------ MMA issuers
+    // One thread per query tile: warp 9 issues tile 0's MMAs, warp 10 tile 1's.  Each
+    // thread's waits then leave the tensor pipe to the other thread's MMAs.
+    const int qi = warp - kWarpMma;
+    const PfWork pw = pf_work(a, NP, G);
+    const SegCtx &sx = pw.sx;
     constexpr uint32_t idS = tc::idesc_f16(128, 128, false);
     constexpr uint32_t idPV = tc::idesc_f16(128, D, true);
     const uint32_t sQ0 = smem_u32(smem + Cfg::kQ0), sQ1 = smem_u32(smem + Cfg::kQ1);
     const uint32_t sK = smem_u32(smem + Cfg::kK), sV = smem_u32(smem + Cfg::kV);
-    // Descriptors of the operand tiles, made once: a k-step moves the start address
-    // (bits 0-13, in 16-byte units) by a constant, and every shared-memory address
-    // here is below 256 KB, so adding to the descriptor never carries out of the field.
+    // Operand descriptors by their low words (the high word is one constant): a k-step
+    // moves the start address (bits 0-13, in 16-byte units) by a constant, and every
+    // shared-memory address here is below 256 KB, so the add never carries out of the
+    // field.  Each group's base goes through opaque() so that its eight descriptors are
+    // formed at issue time, one add each, rather than held in registers.
     static_assert(kPfStages == 2, "two K/V stages");
-    const uint64_t dQ0 = tc::sdesc_sw128(sQ0, 16, 1024), dQ1 = tc::sdesc_sw128(sQ1, 16, 1024);
-    const uint64_t dK0 = tc::sdesc_sw128(sK, 16, 1024);
-    const uint64_t dK1 = tc::sdesc_sw128(sK + Cfg::kTile, 16, 1024);
-    const uint64_t dV0 = tc::sdesc_sw128(sV, kBoxBytes, 1024);
-    const uint64_t dV1 = tc::sdesc_sw128(sV + Cfg::kTile, kBoxBytes, 1024);
+    const uint32_t lQ0 = tc::sdesc_lo(sQ0, 16), lQ1 = tc::sdesc_lo(sQ1, 16);
+    const uint32_t lK0 = tc::sdesc_lo(sK, 16), lK1 = tc::sdesc_lo(sK + Cfg::kTile, 16);
+    const uint32_t lV0 = tc::sdesc_lo(sV, kBoxBytes), lV1 = tc::sdesc_lo(sV + Cfg::kTile, kBoxBytes);
     auto issue_S = [&](int i, int st) {
       const uint32_t d = tmem + i * 128;
-      const uint64_t a0 = i ? dQ1 : dQ0, b0 = st ? dK1 : dK0;
+      const uint32_t a0 = tc::opaque(i ? lQ1 : lQ0), b0 = tc::opaque(st ? lK1 : lK0);
+      tc::mma_ss_lo<0>(d, a0, b0, idS);
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
+      for (int kk = 1; kk < D / 16; ++kk) {
         const uint32_t off16 = ((kk / 4) * kBoxBytes + (kk % 4) * 32) >> 4;
-        if (kk == 0)
-          tc::mma_ss_first(d, a0, b0, idS);
-        else
-          tc::mma_ss_acc(d, a0 + off16, b0 + off16, idS);
+        tc::mma_ss_lo<1>(d, a0 + off16, b0 + off16, idS);
       }
     };
-    auto issue_PV = [&](int i, int st, bool acc) {
+    // O_i (+)= P_i V over the first nk 16-key steps of the block
+    auto issue_PV = [&](int i, int st, bool acc, int nk) {
       const uint32_t d = tmem + 256 + i * D;
       const uint32_t p = tmem + i * 128;
-      const uint64_t b0 = st ? dV1 : dV0;
-      tc::mma_ts(d, p, b0, idPV, acc ? 1u : 0u);
+      const uint32_t b0 = tc::opaque(st ? lV1 : lV0);
+      tc::mma_ts_lo_pred(d, p, b0, idPV, acc ? 1u : 0u);
 #pragma unroll
       for (int kk = 1; kk < KB / 16; ++kk)
-        tc::mma_ts_acc(d, p + kk * 8, b0 + (uint32_t)((kk * 2048) >> 4), idPV);
+        if (kk < nk) tc::mma_ts_lo<1>(d, p + kk * 8, b0 + (uint32_t)((kk * 2048) >> 4), idPV);
     };
-    const bool leader = lane == 0;
     uint32_t it = 0, sc = 0;
     int nitem = 0;
     Seg w;
-    for (bool more = seg_first(w, sx, start, w0, w1); more; more = seg_next(w, sx)) {
+    for (bool more = seg_first(w, sx, pw); more; more = seg_next(w, sx)) {
       const int nseg = w.kb_e - w.kb_b;
       bool ok = pf_wait(&bars->q_full, nitem & 1, err, abort);
       const int st0 = it % kPfStages;
       ok = ok && pf_wait(&bars->k_full[st0], (it / kPfStages) & 1u, err, abort);
       if (!ok) break;
       tc::fence_after_sync();
-      if (leader) {
-        issue_S(0, st0);
-        tc::commit(&bars->s_full[0]);
-        if (NQ == 2) {
-          issue_S(1, st0);
-          tc::commit(&bars->s_full[1]);
-        }
-        tc::commit(&bars->k_empty[st0]);
-      }
-      __syncwarp();
+      issue_S(qi, st0);
+      tc::commit(&bars->s_full[qi]);
+      tc::commit(&bars->k_empty[st0]);
       for (int kk = 0; kk < nseg; ++kk) {
         const int kb = w.kb_b + kk;  // absolute key block
         const uint32_t cur = it + kk;
         const int st = cur % kPfStages;
         const bool last = kk + 1 == nseg;
         if (!pf_wait(&bars->v_full[st], (cur / kPfStages) & 1u, err, abort)) { ok = false; break; }
+        // the item's last block may hold fewer than 128 valid keys: the PV product then
+        // runs only over the 16-key steps that hold valid keys, and the rows of the last
+        // such step past the valid ones are zeroed (P is 0 there, but 0 * NaN is NaN).
+        // Rows are 128 B, so whole rows are zeroed and the swizzle inside a row does not
+        // matter.  Tile 0's issuer zeroes before its PV; tile 1's issues its PV only after
+        // tile 0's turn, which ends after the zeroing.
+        int nk = KB / 16;
         const int nvalid = w.max_kv - kb * KB;
         if (kb + 1 == w.nkb && nvalid < KB) {
-          // zero V rows nvalid..127 in each 64-column box (rows are 128 B, whole rows
-          // are zeroed so the swizzle inside a row does not matter)
-          for (int hf = 0; hf < Cfg::kHalves; ++hf) {
-            uint4 *base = reinterpret_cast<uint4 *>(smem + Cfg::kV + st * Cfg::kTile +
-                                                    hf * kBoxBytes + nvalid * 128);
-            const int n16 = (KB - nvalid) * 8;
-            for (int x = lane; x < n16; x += 32) base[x] = make_uint4(0, 0, 0, 0);
+          nk = (nvalid + 15) / 16;
+          const int n16 = (nk * 16 - nvalid) * 8;
+          if (qi == 0 && n16 > 0) {
+            for (int hf = 0; hf < Cfg::kHalves; ++hf) {
+              uint4 *base = reinterpret_cast<uint4 *>(smem + Cfg::kV + st * Cfg::kTile +
+                                                      hf * kBoxBytes + nvalid * 128);
+              for (int x = 0; x < n16; ++x) base[x] = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async();
           }
-          fence_proxy_async();
         }
-        __syncwarp();
-        if (!pf_wait(&bars->p_full[0], (sc + kk) & 1u, err, abort)) { ok = false; break; }
-        if (kk == 0 && nitem > 0 && !pf_wait(&bars->o_empty[0], (nitem - 1) & 1, err, abort)) {
+        if (!pf_wait(&bars->p_full[qi], (sc + kk) & 1u, err, abort)) { ok = false; break; }
+        if (kk == 0 && nitem > 0 && !pf_wait(&bars->o_empty[qi], (nitem - 1) & 1, err, abort)) {
+          ok = false;
+          break;
+        }
+        // every wait of the block comes before its MMAs, so that PV_i(kb) and S_i(kb+1)
+        // go to the tensor pipe as one burst of 16 (a wait between them would leave the
+        // pipe idle: each costs ~100 cycles even when the phase has completed)
+        const uint32_t nxt = cur + 1;
+        const int st2 = nxt % kPfStages;
+        if (!last && !pf_wait(&bars->k_full[st2], (nxt / kPfStages) & 1u, err, abort)) {
+          ok = false;
+          break;
+        }
+        // strict alternation of the two issuers, block by block: tile 0's PV(kb), S(kb+1),
+        // then tile 1's, then tile 0's PV(kb+1) ...  A thread waits for its turn while the
+        // other's MMAs run, and the two softmax warpgroups stay half a period apart.
+        if (NQ == 2 && (qi == 1 || cur > 0) &&
+            !pf_wait(&bars->turn[qi], (qi ? cur : cur - 1) & 1u, err, abort)) {
           ok = false;
           break;
         }
         tc::fence_after_sync();
-        if (leader) {
-          issue_PV(0, st, kk > 0);
-          if (last) tc::commit(&bars->o_full[0]);
-        }
-        __syncwarp();
-        int st2 = 0;
+        issue_PV(qi, st, kk > 0, nk);
+        if (last) tc::commit(&bars->o_full[qi]);
+        tc::commit(&bars->v_empty[st]);
         if (!last) {
-          const uint32_t nxt = cur + 1;
-          st2 = nxt % kPfStages;
-          if (!pf_wait(&bars->k_full[st2], (nxt / kPfStages) & 1u, err, abort)) { ok = false; break; }
-          tc::fence_after_sync();
-          if (leader) {
-            issue_S(0, st2);
-            tc::commit(&bars->s_full[0]);
-          }
-          __syncwarp();
+          issue_S(qi, st2);
+          tc::commit(&bars->s_full[qi]);
+          tc::commit(&bars->k_empty[st2]);
         }
-        if (NQ == 2) {
-          if (!pf_wait(&bars->p_full[1], (sc + kk) & 1u, err, abort)) { ok = false; break; }
-          if (kk == 0 && nitem > 0 && !pf_wait(&bars->o_empty[1], (nitem - 1) & 1, err, abort)) {
-            ok = false;
-            break;
-          }
-          tc::fence_after_sync();
-          if (leader) {
-            issue_PV(1, st, kk > 0);
-            if (last) tc::commit(&bars->o_full[1]);
-          }
-        }
-        if (leader) {
-          tc::commit(&bars->v_empty[st]);
-          if (!last) {
-            if (NQ == 2) {
-              issue_S(1, st2);
-              tc::commit(&bars->s_full[1]);
-            }
-            tc::commit(&bars->k_empty[st2]);
-          }
-        }
-        __syncwarp();
+        if (NQ == 2) mbar_arrive(&bars->turn[qi ^ 1]);
       }
       if (!ok) break;
-      if (leader) tc::commit(&bars->q_empty);
-      __syncwarp();
+      tc::commit(&bars->q_empty);
       it += nseg;
       sc += nseg;
       ++nitem;
@@ -413,12 +483,16 @@ k_prefill(AttnArgs a, const __grid_constant__ AttnMaps maps) {
     const uint32_t tS = tmem + wg * 128 + lane_off;
     const uint32_t tO = tmem + 256 + wg * D + lane_off;
     if (wg < NQ) {
+      const PfWork pw = pf_work(a, NP, G);
+      const SegCtx &sx = pw.sx;
+      const long long W = pw.W, w0 = pw.w0;
+      const int C = pw.C;
       uint32_t sc = 0;
       int nitem = 0;
       float *parts = reinterpret_cast<float *>(a.ws + a.lay.partials);
       int *cnt = reinterpret_cast<int *>(a.ws + a.lay.pf_cnt);
       Seg w;
-      for (bool more = seg_first(w, sx, start, w0, w1); more; more = seg_next(w, sx)) {
+      for (bool more = seg_first(w, sx, pw); more; more = seg_next(w, sx)) {
         const int h = wg ? w.h1 : w.h0;
         const int tok = w.tile_start + row;
         const bool valid = row < w.n_tok;
@@ -427,35 +501,42 @@ k_prefill(AttnArgs a, const __grid_constant__ AttnMaps maps) {
         const int nseg = w.kb_e - w.kb_b;
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
+        const bool split = w.kb_b != 0 || w.kb_e != w.nkb;
         for (int kk = 0; kk < nseg; ++kk) {
           const int kb = w.kb_b + kk;
+          if (split && kk + 1 == nseg && wl == 0 && lane == 0) {
+            // the records of the item's other parts, which this warpgroup may combine
+            // after this block: into L2 now (one written long ago may have left it)
+            const long long ie = w.item_start + w.nkb;
+            for (int cc = cta_of_unit(w.item_start, W, C); cc <= cta_of_unit(ie - 1, W, C); ++cc)
+              if (cc != c && cta_has_units(cc, W, C))
+                bulk_prefetch_l2(parts + ((size_t)(2 * cc + (w.item_start <= (long long)cc * W / C
+                                                                  ? 0 : 1)) * 2 + wg) *
+                                             (size_t)kPartStride * 128,
+                                 kPartStride * 128 * 4);
+          }
           if (!pf_wait(&bars->s_full[wg], (sc + kk) & 1u, err, abort)) { ok = false; break; }
           tc::fence_after_sync();
           const int nv = min(max(L - kb * KB, 0), KB);  // valid keys of this row here
           const bool wfull = __all_sync(0xffffffffu, nv == KB);
-          // pass 1: row max of the raw scores over the valid keys, 64 columns at a time
-          // (scale > 0 commutes with max).  Masked scores become -inf by select, so
-          // NaN cells never propagate.
+          // The whole 128-column score row in one TMEM round trip (the tensor core keeps
+          // TMEM busy, so each round trip costs hundreds of cycles).  Row max of the raw
+          // scores over the valid keys (scale > 0 commutes with max); masked scores become
+          // -inf by select, so NaN cells never propagate.
+          uint32_t t[128];
+          tc::ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(t));
+          tc::ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(t + 32));
+          tc::ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(t + 64));
+          tc::ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(t + 96));
+          tc::wait_ld();
+          if (!wfull) {
+#pragma unroll
+            for (int j = 0; j < 128; ++j) t[j] = j < nv ? t[j] : 0xff800000u;  // -inf
+          }
           float mx = -INFINITY;
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            uint32_t t0[32], t1[32];
-            tc::ld32(tS + 64 * hh, t0);
-            tc::ld32(tS + 64 * hh + 32, t1);
-            tc::wait_ld();
-            if (wfull) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j)
-                mx = fmax3(mx, __uint_as_float(t0[j]), __uint_as_float(t1[j]));
-            } else {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                const int k0 = 64 * hh + j;
-                mx = fmax3(mx, k0 < nv ? __uint_as_float(t0[j]) : -INFINITY,
-                           k0 + 32 < nv ? __uint_as_float(t1[j]) : -INFINITY);
-              }
-            }
-          }
+          for (int j = 0; j < 128; j += 2)
+            mx = fmax3(mx, __uint_as_float(t[j]), __uint_as_float(t[j + 1]));
           const float m_new = fmaxf(m_run, mx * a.scale_log2);
           const bool need = m_new > m_run + kRescaleThreshold;
           float alpha = 1.f;
@@ -463,36 +544,30 @@ k_prefill(AttnArgs a, const __grid_constant__ AttnMaps maps) {
             alpha = exp2_approx(m_run - m_new);
             m_run = m_new;
           }
-          // pass 2: p = 2^(s * scale_log2 - m), one packed FMA per pair, then ex2; a row
-          // with no valid key yet uses m = 0 so that its -inf scores give exactly 0.
-          // P (f16) goes to the first 64 columns of S: half hh lands in columns
-          // [32hh, 32hh+32), below the columns half hh+1 still has to read.
+          // p = 2^(s * scale_log2 - m), one packed FMA per pair, then ex2; a row with no
+          // valid key yet uses m = 0 so that its -inf scores give exactly 0.  P (f16) goes
+          // to the first 64 columns of S (already in registers): half hh lands in columns
+          // [32hh, 32hh+32).
           const float m_use = m_run == -INFINITY ? 0.f : m_run;
           const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
           const float2 nm2 = make_float2(-m_use, -m_use);
-          float rs = 0.f;
+          float2 rs2 = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            uint32_t t[64];
-            tc::ld32(tS + 64 * hh, *reinterpret_cast<uint32_t(*)[32]>(t));
-            tc::ld32(tS + 64 * hh + 32, *reinterpret_cast<uint32_t(*)[32]>(t + 32));
-            tc::wait_ld();
-            uint32_t pk[32];
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t pk[16];
 #pragma unroll
-            for (int j = 0; j < 64; j += 2) {
-              float2 x = ffma2(make_float2(__uint_as_float(t[j]), __uint_as_float(t[j + 1])),
-                               sc2, nm2);
-              if (!wfull) {
-                x.x = 64 * hh + j < nv ? x.x : -INFINITY;
-                x.y = 64 * hh + j + 1 < nv ? x.y : -INFINITY;
-              }
-              const float p0 = exp2_approx(x.x), p1 = exp2_approx(x.y);
-              rs += p0 + p1;
-              __half2 hp = __floats2half2_rn(p0, p1);
+            for (int j = 0; j < 32; j += 2) {
+              const int c = 32 * q4 + j;
+              const float2 x =
+                  ffma2(make_float2(__uint_as_float(t[c]), __uint_as_float(t[c + 1])), sc2, nm2);
+              const float2 p = make_float2(exp2_approx(x.x), exp2_approx(x.y));
+              rs2 = fadd2(rs2, p);
+              __half2 hp = __floats2half2_rn(p.x, p.y);
               pk[j >> 1] = *reinterpret_cast<uint32_t *>(&hp);
             }
-            tc::st32(tS + 32 * hh, pk);
+            tc::st16(tS + 16 * q4, pk);
           }
+          const float rs = rs2.x + rs2.y;
           l_run = l_run * alpha + rs;
           if (kk > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
@@ -515,45 +590,45 @@ k_prefill(AttnArgs a, const __grid_constant__ AttnMaps maps) {
         if (w.kb_b == 0 && w.kb_e == w.nkb) {
           // the whole item: normalise and store f16
           const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+          uint32_t o[D];  // the whole O row in one TMEM round trip
 #pragma unroll
-          for (int ch = 0; ch < D / 32; ++ch) {
-            uint32_t o[32];
-            tc::ld32(tO + ch * 32, o);
-            tc::wait_ld();
-            if (valid) {
+          for (int ch = 0; ch < D / 32; ++ch)
+            tc::ld32(tO + ch * 32, *reinterpret_cast<uint32_t(*)[32]>(o + ch * 32));
+          tc::wait_ld();
+          if (valid) {
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                uint32_t hw[4];
+            for (int q = 0; q < D / 8; ++q) {
+              uint32_t hw[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  __half2 hv = __floats2half2_rn(__uint_as_float(o[q * 8 + 2 * e]) * inv,
-                                                 __uint_as_float(o[q * 8 + 2 * e + 1]) * inv);
-                  hw[e] = *reinterpret_cast<uint32_t *>(&hv);
-                }
-                orow[ch * 4 + q] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+              for (int e = 0; e < 4; ++e) {
+                __half2 hv = __floats2half2_rn(__uint_as_float(o[q * 8 + 2 * e]) * inv,
+                                               __uint_as_float(o[q * 8 + 2 * e + 1]) * inv);
+                hw[e] = *reinterpret_cast<uint32_t *>(&hv);
               }
+              orow[q] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
             }
           }
           tc::fence_before_sync();
           mbar_arrive(&bars->o_empty[wg]);
         } else {
-          // one part of a split item: leave (O unnormalised, m, l) in this CTA's slot
+          // one part of a split item: leave (O unnormalised, m, l) in this CTA's slot.  A
+          // slot holds D + 2 rows of 128 floats (element-major: element e of query row r
+          // at [e][r]), so that a warp's accesses to one element are one 128-byte line.
           const bool first_seg = w.item_start <= w0;
           const int my_slot = 2 * c + (first_seg ? 0 : 1);
-          float *rec = parts + (((size_t)my_slot * 2 + wg) * 128 + row) * kPartStride;
+          auto slot_base = [&](int sl) {
+            return parts + ((size_t)sl * 2 + wg) * (size_t)kPartStride * 128 + row;
+          };
+          float *rec = slot_base(my_slot);
+          uint32_t o[D];
 #pragma unroll
-          for (int ch = 0; ch < D / 32; ++ch) {
-            uint32_t o[32];
-            tc::ld32(tO + ch * 32, o);
-            tc::wait_ld();
+          for (int ch = 0; ch < D / 32; ++ch)
+            tc::ld32(tO + ch * 32, *reinterpret_cast<uint32_t(*)[32]>(o + ch * 32));
+          tc::wait_ld();
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-              reinterpret_cast<float4 *>(rec + ch * 32)[q] =
-                  make_float4(__uint_as_float(o[4 * q]), __uint_as_float(o[4 * q + 1]),
-                              __uint_as_float(o[4 * q + 2]), __uint_as_float(o[4 * q + 3]));
-          }
-          rec[D] = m_run;
-          rec[D + 1] = l_run;
+          for (int e = 0; e < D; ++e) rec[e * 128] = __uint_as_float(o[e]);
+          rec[D * 128] = m_run;
+          rec[(D + 1) * 128] = l_run;
           tc::fence_before_sync();
           mbar_arrive(&bars->o_empty[wg]);
           // count the parts that have landed; the last one combines (no waiting)
@@ -571,45 +646,51 @@ k_prefill(AttnArgs a, const __grid_constant__ AttnMaps maps) {
           old = __shfl_sync(0xffffffffu, old, 0);
           if (old == n_parts - 1) {
             __threadfence();
-            // the other parts were written by other SMs: read them past L1 (ld.global.cg)
+            // The other parts were written by other SMs: read them past L1 (ld.global.cg).
+            // This CTA's own part is still in registers.  Parts are folded in CTA order
+            // with the same arithmetic whichever CTA combines, so results are reproducible.
+            auto slot_of = [&](int cc) {
+              return 2 * cc + (w.item_start <= (long long)cc * W / C ? 0 : 1);
+            };
             float M = -INFINITY;
             for (int cc = c1; cc <= c2; ++cc) {
               if (!cta_has_units(cc, W, C)) continue;
-              const int sl = 2 * cc + (w.item_start <= (long long)cc * W / C ? 0 : 1);
-              M = fmaxf(M, __ldcg(parts + (((size_t)sl * 2 + wg) * 128 + row) * kPartStride + D));
+              M = fmaxf(M, cc == c ? m_run : __ldcg(slot_base(slot_of(cc)) + D * 128));
             }
             float Ls = 0.f;
             for (int cc = c1; cc <= c2; ++cc) {
               if (!cta_has_units(cc, W, C)) continue;
-              const int sl = 2 * cc + (w.item_start <= (long long)cc * W / C ? 0 : 1);
-              const float *r = parts + (((size_t)sl * 2 + wg) * 128 + row) * kPartStride;
-              const float m_p = __ldcg(r + D);
-              Ls += (m_p == -INFINITY) ? 0.f : __ldcg(r + D + 1) * exp2_approx(m_p - M);
+              const float *r = slot_base(slot_of(cc));
+              const float m_p = cc == c ? m_run : __ldcg(r + D * 128);
+              const float l_p = cc == c ? l_run : __ldcg(r + (D + 1) * 128);
+              Ls += (m_p == -INFINITY) ? 0.f : l_p * exp2_approx(m_p - M);
             }
             const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-#pragma unroll 1
-            for (int ch = 0; ch < D / 32; ++ch) {
-              float acc[32];
 #pragma unroll
-              for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+            for (int ch = 0; ch < D / 16; ++ch) {
+              float acc[16];
+#pragma unroll
+              for (int e = 0; e < 16; ++e) acc[e] = 0.f;
               for (int cc = c1; cc <= c2; ++cc) {
                 if (!cta_has_units(cc, W, C)) continue;
-                const int sl = 2 * cc + (w.item_start <= (long long)cc * W / C ? 0 : 1);
-                const float *r = parts + (((size_t)sl * 2 + wg) * 128 + row) * kPartStride;
-                const float m_p = __ldcg(r + D);
-                const float f = (m_p == -INFINITY) ? 0.f : exp2_approx(m_p - M);
+                if (cc == c) {
+                  const float f = (m_run == -INFINITY) ? 0.f : exp2_approx(m_run - M);
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                  const float4 v4 = __ldcg(reinterpret_cast<const float4 *>(r + ch * 32) + q);
-                  acc[4 * q] += f * v4.x;
-                  acc[4 * q + 1] += f * v4.y;
-                  acc[4 * q + 2] += f * v4.z;
-                  acc[4 * q + 3] += f * v4.w;
+                  for (int e = 0; e < 16; ++e) acc[e] += f * __uint_as_float(o[ch * 16 + e]);
+                } else {
+                  const float *r = slot_base(slot_of(cc));
+                  float v[16];
+                  const float m_p = __ldcg(r + D * 128);
+#pragma unroll
+                  for (int e = 0; e < 16; ++e) v[e] = __ldcg(r + (ch * 16 + e) * 128);
+                  const float f = (m_p == -INFINITY) ? 0.f : exp2_approx(m_p - M);
+#pragma unroll
+                  for (int e = 0; e < 16; ++e) acc[e] += f * v[e];
                 }
               }
               if (valid) {
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
+                for (int q = 0; q < 2; ++q) {
                   uint32_t hw[4];
 #pragma unroll
                   for (int e = 0; e < 4; ++e) {
@@ -617,7 +698,7 @@ k_prefill(AttnArgs a, const __grid_constant__ AttnMaps maps) {
                                                    acc[q * 8 + 2 * e + 1] * inv);
                     hw[e] = *reinterpret_cast<uint32_t *>(&hv);
                   }
-                  orow[ch * 4 + q] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                  orow[ch * 2 + q] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
                 }
               }
             }
@@ -631,9 +712,8 @@ k_prefill(AttnArgs a, const __grid_constant__ AttnMaps maps) {
   }
 
   __syncthreads();
-  if (*abort && warp == kWarpMma && lane == 0) {
+  if (*abort && (warp == kWarpMma || warp == kWarpMma + 1) && lane == 0) {
     // a role gave up: let the tensor pipe drain (bounded) before TMEM is freed
-    tc::commit(&bars->q_empty);
     uint64_t t0 = globaltimer_ns();
     while (globaltimer_ns() - t0 < 1000000ull) {
     }

@@ -392,7 +392,18 @@ k_plan(const int32_t *__restrict__ tpt, int max_pages, const int32_t *__restrict
       int nkb = tiles[t].z;
       long long r = w - tile_off[t];
       int j = nkb > 0 ? (int)(r / nkb) : 0;
-      pf_start[c] = make_int4(t, j, nkb > 0 ? (int)(r - (long long)j * nkb) : 0, 0);
+      // and the item holding the CTA's last unit, tile * Hkv * NP + item (the prefill
+      // kernel runs the segment of that item first, so that both parts of every split
+      // item are done early and their combine stays off the end of the launch)
+      long long wl = (long long)(c + 1) * W / C - 1;
+      if (wl < w) wl = w;
+      int tl = upper_index(tile_off, tile_base, wl, 1);
+      if (tl >= tile_base) tl = tile_base - 1;
+      while (tiles[tl].z == 0 && tl + 1 < tile_base) ++tl;
+      const int nkl = tiles[tl].z;
+      const int jl = nkl > 0 ? (int)((wl - tile_off[tl]) / nkl) : 0;
+      pf_start[c] = make_int4(t, j, nkb > 0 ? (int)(r - (long long)j * nkb) : 0,
+                              tl * Hkv * NP + jl);
     }
   }
   if (tid == 0) {
