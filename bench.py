@@ -601,6 +601,75 @@ def bench_unified_span(pa, torch, db, steps, warmup, world, hbm, paged_ms_per_la
             "timing": "CUDA graph of one plan and 36 masked decode launches (one per layer)"}
 
 
+def bench_unified_span_prefill(pa, torch, pb, steps, warmup, world, paged_ms_per_step):
+    """The unified-span baseline of the headline prefill: every ubatch of the 8x16K step
+    attends over the span of the whole pool (every token's row names all 1280 pages,
+    kv_len = the span) under the per-cell (sequence, position) mask, on the same tcgen05
+    tiles; against the paged step.  Runs on the pool after the timed paged steps (every
+    owned cell written); the cell map is the final one (positions past a token's own
+    are masked as in the paged kernel)."""
+    wl, dev = pb.wl, pb.kp.device
+    N, P = wl.num_pages, wl.P
+    cs = np.full(N * P, -1, np.int32)
+    cp = np.full(N * P, -1, np.int32)
+    for s_ in range(wl.n_seq):
+        pos = np.arange(wl.seq_len)
+        slots = wl.seq_page_table[s_][pos // P].astype(np.int64) * P + pos % P
+        cs[slots], cp[slots] = s_, pos
+    Tmax = max(d["T"] for d in pb.ub)
+    tpt = torch.arange(N, dtype=torch.int32, device=dev).repeat(Tmax, 1).contiguous()
+    kv = torch.full((Tmax,), N * P, dtype=torch.int32, device=dev)
+    cs_d, cp_d = torch.from_numpy(cs).to(dev), torch.from_numpy(cp).to(dev)
+    ws = pa.new_workspace(Tmax, wl.Hq, wl.Hkv, wl.d, dev)
+    out = torch.empty((Tmax, wl.Hq, wl.d), dtype=torch.float16, device=dev)
+
+    def step():
+        for d in pb.ub:
+            T = d["T"]
+            pa.plan_prefill(tpt[:T], kv[:T], wl.Hq, wl.Hkv, P, wl.d, ws)
+            pa.masked_prefill(d["q"], pb.kp, pb.vp, tpt[:T], kv[:T], wl.scale, cs_d, cp_d,
+                              d["tok_seq"], d["tok_pos"], out[:T], ws)
+
+    g = capture_step(torch, step)
+    n_steps = max(1, min(steps, 3))
+    total_ms, _ = time_steps(torch, g.replay, n_steps, min(warmup, 1), world)
+    ms = max_over_ranks(total_ms / n_steps, world)
+    if pa.read_error(ws):
+        raise RuntimeError("device error word set in the unified-span prefill")
+    # the last ubatch of the span step against the paged output of the same ubatch
+    last = pb.ub[-1]
+    diff = (out[:last["T"]].float() - last["out"].float()).abs()
+    tol = 2e-3 + 1e-2 * last["out"].float().abs()
+    agree = bool((diff <= 2 * tol).all())
+    # K/V bytes each kernel streams and the MMA work it does: a tile item reads every key
+    # block up to its longest kv_len (paged) or the whole span (unified)
+    G = wl.Hq // wl.Hkv
+    items_per_tile = wl.Hkv * max(1, G // 2)
+    blk_bytes = 128 * wl.d * 2 * 2
+    paged_blocks = span_blocks = 0
+    for u in range(len(pb.ub)):
+        ts_, tp_ = wl.ubatches[u]
+        cut = np.flatnonzero(np.diff(ts_)) + 1
+        for a_, b_ in zip(np.concatenate([[0], cut]), np.concatenate([cut, [len(ts_)]])):
+            n = b_ - a_
+            nt = -(-n // 128)
+            for i in range(nt):
+                lo, hi = a_ + n * i // nt, a_ + n * (i + 1) // nt
+                paged_blocks += items_per_tile * -(-int(tp_[lo:hi].max() + 1) // 128)
+        span_blocks += items_per_tile * -(-len(ts_) // 128) * (N * P // 128)
+    return {"workload": "prefill_8x16k_unified_span", "unit": "ms", "value": round(ms, 3),
+            "higher_is_better": False, "ms_per_step": round(ms, 3),
+            "paged_ms_per_step": round(paged_ms_per_step, 3),
+            "paged_speedup": round(ms / paged_ms_per_step, 2),
+            "kv_bytes_per_step": {"span": span_blocks * blk_bytes, "paged": paged_blocks * blk_bytes},
+            "bytes_ratio": round(span_blocks / paged_blocks, 2),
+            "tflops_equiv": round(pb.flops / (ms / 1e3) / 1e12, 2),
+            "agrees_with_paged_on_last_ubatch": agree,
+            "timing": f"CUDA graph of 65 x (plan + masked tcgen05 prefill), {n_steps} step(s)",
+            "note": "the span is every cell of the pool (free cells masked, their V rows zeroed); "
+                    "llama.cpp's unified cache reads the span the same way"}
+
+
 def bench_fp8_decode(pa, torch, db, steps, warmup, world, hbm, f16_ms_per_layer):
     """FP8 KV pages on the decode workload: the same 36 layers with every cached row
     quantised (E4M3 codes, one scale per row) by the library's quantising append;
@@ -901,6 +970,8 @@ def run_ours(args):
             with_cpu=rank == 0 and world == 1 and not args.no_cpu_baseline, seed=args.seed),
         "unified_span": bench_unified_span(pa, torch, db, args.steps, args.warmup, world, hbm,
                                            d_kt * 1e3),
+        "unified_span_prefill": bench_unified_span_prefill(pa, torch, pb, args.steps,
+                                                           args.warmup, world, t_step * 1e3),
         "fp8_pages": bench_fp8_decode(pa, torch, db, args.steps, args.warmup, world, hbm,
                                       d_kt * 1e3),
     }

@@ -19,7 +19,8 @@
  *  around it:  paged_attn_workspace_size, paged_attn_validate,
  *              paged_attn_read_error, paged_attn_strerror, paged_attn_version,
  *              paged_attn_set_prefill_min_run, pa_pool_* (host page pool)
- *  beyond it:  paged_attn_plan_decode; paged_attn_masked_decode (the
+ *  beyond it:  paged_attn_plan_decode, paged_attn_plan_prefill;
+ *              paged_attn_masked_decode and paged_attn_masked_prefill (the
  *              unified-span baseline that paging replaces); paged_kv_append_fp8
  *              and paged_attn_decode_fp8 (FP8 pages); paged_copy_pages and
  *              pa_pool_fork (copy-on-write forks of shared pages)
@@ -253,6 +254,39 @@ int paged_attn_masked_decode(const uint16_t *q, const uint16_t *k_pages, const u
                              const int32_t *cell_pos, const int32_t *tok_seq,
                              const int32_t *tok_pos, uint16_t *out, void *workspace,
                              size_t workspace_bytes, void *stream);
+
+/*
+ * paged_attn_plan with every token routed to the tensor-core tiles (none to the
+ * split-KV path): the plan that paged_attn_masked_prefill runs on.  Arguments as
+ * paged_attn_plan.
+ */
+int paged_attn_plan_prefill(const int32_t *tok_page_table, int max_pages,
+                            const int32_t *tok_kv_len, int T, int Hq, int Hkv, int P, int d,
+                            void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Unified-span baseline for prefill (UA-PagedAttention page, section 作品简介: the
+ * original cache is one span of cells shared by all sequences, read whole under a
+ * mask; section 关键性能数据 measures the prefill of 16K prompts x 8 against it).
+ * The same computation as paged_attn_masked_decode, on the tcgen05 prefill tiles:
+ * every token attends to the keys its table row names, keeping only key j whose slot
+ * s = page * P + j % P holds a cell of the token's own sequence at a position up to
+ * its own (cell_seq[s] == tok_seq[t] and cell_pos[s] <= tok_pos[t]).  With every row
+ * naming the whole span and kv_len = the span length, consecutive tokens share a tile
+ * whatever their sequence, and each tile streams the whole span.
+ *   Arguments as paged_attn_masked_decode.  Runs on the workspace's plan, which must
+ *   come from paged_attn_plan_prefill (every token in a tile) for the same tables;
+ *   writes out for every token.  A cell with cell_seq >= 0 must hold written (finite)
+ *   K/V; the V rows of free cells (cell_seq < 0) are zeroed in shared memory, so their
+ *   contents never matter.  A token whose mask keeps no key gets a zero row.
+ */
+int paged_attn_masked_prefill(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
+                              const int32_t *tok_page_table, int max_pages,
+                              const int32_t *tok_kv_len, int T, int Hq, int Hkv, int P, int d,
+                              int num_pages, float scale, const int32_t *cell_seq,
+                              const int32_t *cell_pos, const int32_t *tok_seq,
+                              const int32_t *tok_pos, uint16_t *out, void *workspace,
+                              size_t workspace_bytes, void *stream);
 
 /*
  * Reduced-precision KV pages: FP8 E4M3 codes with one binary32 scale per cached

@@ -11,7 +11,8 @@ Entry points mirror include/paged_attn.h:
   expand_ubatch   per-token page-table / kv_len expansion + slot mapping
   kv_append       reshape-and-cache into the paged pool
   copy_pages      page copy of a copy-on-write fork
-  masked_decode   the unified-span baseline (masked attention over a shared span)
+  masked_decode / masked_prefill   the unified-span baseline (masked attention over a
+                  shared span) on the split-KV and on the tcgen05 path
   kv_append_fp8 / decode_fp8   FP8 (E4M3) KV pages with per-row scales
   plan / prefill / decode / run / forward   the attention itself
   validate, read_error, set_prefill_min_run, workspace_size
@@ -71,6 +72,9 @@ _SIGS = {
     "paged_attn_plan_decode": ([_vp, _i, _vp, _i, _i, _i, _i, _i, _vp, _sz, _vp], _i),
     "paged_attn_masked_decode": ([_vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i,
                                   ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i),
+    "paged_attn_plan_prefill": ([_vp, _i, _vp, _i, _i, _i, _i, _i, _vp, _sz, _vp], _i),
+    "paged_attn_masked_prefill": ([_vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i,
+                                   ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i),
 }
 for _name, (_args, _res) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -168,11 +172,35 @@ def plan_decode(tok_page_table, tok_kv_len, Hq, Hkv, P, d, workspace, stream=Non
                                        _stream(stream)), "paged_attn_plan_decode")
 
 
+def plan_prefill(tok_page_table, tok_kv_len, Hq, Hkv, P, d, workspace, stream=None):
+    """plan with every token in a tensor-core tile (for masked_prefill)."""
+    _req(tok_page_table, torch.int32, "tok_page_table")
+    _req(tok_kv_len, torch.int32, "tok_kv_len")
+    T, max_pages = tok_page_table.shape
+    _check(_lib.paged_attn_plan_prefill(_ptr(tok_page_table), max_pages, _ptr(tok_kv_len), T, Hq,
+                                        Hkv, P, d, _ptr(workspace), workspace.numel(),
+                                        _stream(stream)), "paged_attn_plan_prefill")
+
+
 def masked_decode(q, k_pages, v_pages, tok_page_table, tok_kv_len, scale, cell_seq, cell_pos,
                   tok_seq, tok_pos, out, workspace, stream=None):
     """Unified-span baseline: split-KV attention of every token over its row, keeping
     only the slots whose cell belongs to the token's sequence at a position up to its
     own.  Runs on a plan from plan_decode."""
+    return _masked("paged_attn_masked_decode", q, k_pages, v_pages, tok_page_table, tok_kv_len,
+                   scale, cell_seq, cell_pos, tok_seq, tok_pos, out, workspace, stream)
+
+
+def masked_prefill(q, k_pages, v_pages, tok_page_table, tok_kv_len, scale, cell_seq, cell_pos,
+                   tok_seq, tok_pos, out, workspace, stream=None):
+    """The same masked attention on the tcgen05 prefill tiles (the unified-span
+    baseline of prefill).  Runs on a plan from plan_prefill."""
+    return _masked("paged_attn_masked_prefill", q, k_pages, v_pages, tok_page_table, tok_kv_len,
+                   scale, cell_seq, cell_pos, tok_seq, tok_pos, out, workspace, stream)
+
+
+def _masked(fn_name, q, k_pages, v_pages, tok_page_table, tok_kv_len, scale, cell_seq, cell_pos,
+            tok_seq, tok_pos, out, workspace, stream):
     for t, n in ((q, "q"), (k_pages, "k_pages"), (v_pages, "v_pages"), (out, "out")):
         _req(t, torch.float16, n)
     for t, n in ((tok_page_table, "tok_page_table"), (tok_kv_len, "tok_kv_len"),
@@ -182,11 +210,10 @@ def masked_decode(q, k_pages, v_pages, tok_page_table, tok_kv_len, scale, cell_s
     T, Hq, d = q.shape
     N, Hkv, P, _ = k_pages.shape
     max_pages = tok_page_table.shape[1]
-    _check(_lib.paged_attn_masked_decode(
+    _check(getattr(_lib, fn_name)(
         _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(tok_page_table), max_pages, _ptr(tok_kv_len),
         T, Hq, Hkv, P, d, N, float(scale), _ptr(cell_seq), _ptr(cell_pos), _ptr(tok_seq),
-        _ptr(tok_pos), _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)),
-        "paged_attn_masked_decode")
+        _ptr(tok_pos), _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)), fn_name)
     return out
 
 

@@ -271,6 +271,38 @@ int paged_attn_plan_decode(const int32_t *tok_page_table, int max_pages,
                    workspace_bytes, stream, INT_MAX);
 }
 
+int paged_attn_plan_prefill(const int32_t *tok_page_table, int max_pages,
+                            const int32_t *tok_kv_len, int T, int Hq, int Hkv, int P, int d,
+                            void *workspace, size_t workspace_bytes, void *stream) {
+  NvtxRange nvtx_range("paged_attn_plan_prefill");
+  return plan_with(tok_page_table, max_pages, tok_kv_len, T, Hq, Hkv, P, d, workspace,
+                   workspace_bytes, stream, 1);
+}
+
+int paged_attn_masked_prefill(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
+                              const int32_t *tok_page_table, int max_pages,
+                              const int32_t *tok_kv_len, int T, int Hq, int Hkv, int P, int d,
+                              int num_pages, float scale, const int32_t *cell_seq,
+                              const int32_t *cell_pos, const int32_t *tok_seq,
+                              const int32_t *tok_pos, uint16_t *out, void *workspace,
+                              size_t workspace_bytes, void *stream) {
+  NvtxRange nvtx_range("paged_attn_masked_prefill");
+  int st = check_attn(q, k_pages, v_pages, tok_page_table, max_pages, tok_kv_len, T, Hq, Hkv, P, d,
+                      num_pages, out, workspace, workspace_bytes, true);
+  if (st != PA_OK || T == 0) return st;
+  if (!cell_seq || !cell_pos || !tok_seq || !tok_pos) return PA_EINVAL;
+  AttnArgs a = make_args(q, k_pages, v_pages, tok_page_table, max_pages, tok_kv_len, T, Hq, Hkv, P,
+                         d, num_pages, scale, out, workspace);
+  a.cell_seq = cell_seq;
+  a.cell_pos = cell_pos;
+  a.tok_seq = tok_seq;
+  a.tok_pos = tok_pos;
+  AttnMaps maps;
+  st = encode_attn_maps(a, &maps);
+  if (st != PA_OK) return st;
+  return launch_status(launch_prefill(a, sm_count(), &maps, static_cast<cudaStream_t>(stream)));
+}
+
 int paged_attn_masked_decode(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
                              const int32_t *tok_page_table, int max_pages,
                              const int32_t *tok_kv_len, int T, int Hq, int Hkv, int P, int d,

@@ -64,7 +64,10 @@ struct PfCfg {
   static constexpr int kK = 2 * kTile;
   static constexpr int kV = kK + kPfStages * kTile;
   static constexpr int kBarOff = kV + kPfStages * kTile;
-  static constexpr int kUsed = kBarOff + 256;
+  // masked variant: (sequence, position) of each key of the block, per softmax
+  // warpgroup, two buffers
+  static constexpr int kCinfo = kBarOff + 256;
+  static constexpr int kUsed = kCinfo + 2 * 2 * 128 * 8;
   // at least ~120 KB so that a second CTA never shares the SM (and its TMEM)
   static constexpr int kSmem = (kUsed < 120 * 1024 ? 120 * 1024 : kUsed) + 1024;
 };
@@ -208,7 +211,11 @@ __device__ __forceinline__ bool seg_first(Seg &s, const SegCtx &x, const PfWork 
   return seg_begin(s, x, pw.start, pw.w0, pw.w1);
 }
 
-template <int D>
+// MASK: the unified-span baseline.  Every tile token's row names the same span of
+// cells; key j is kept only if its cell belongs to the token's sequence at a position
+// up to the token's own (cell_seq[slot] == tok_seq[t] && cell_pos[slot] <= tok_pos[t]),
+// and the V rows of free cells (cell_seq < 0, which may hold NaN) are zeroed.
+template <int D, bool MASK>
 __global__ void __launch_bounds__(kPfThreads, 1)
 k_prefill(AttnArgs a, const __grid_constant__ AttnMaps maps) {
   using Cfg = PfCfg<D>;
@@ -497,6 +504,19 @@ k_prefill(AttnArgs a, const __grid_constant__ AttnMaps maps) {
         const int tok = w.tile_start + row;
         const bool valid = row < w.n_tok;
         const int L = valid ? min(max(a.kv[tok], 0), cap) : 0;
+        // masked variant: this row's (sequence, position); -2 matches no cell
+        const int my_seq = MASK && valid ? a.tok_seq[tok] : -2;
+        const int my_pos = MASK && valid ? a.tok_pos[tok] : -1;
+        // (sequence, position) of key `row` of block kb of this item; -1 past the keys
+        auto cell_of = [&](int kb) -> int2 {
+          const int key = kb * KB + row;
+          if (!MASK || kb >= w.nkb || key >= w.max_kv) return make_int2(-1, 0);
+          const int page = a.tpt[(size_t)w.tile_start * a.max_pages + key / a.P];
+          if (page < 0 || page >= a.num_pages) return make_int2(-1, 0);
+          const size_t slot = (size_t)page * a.P + key % a.P;
+          return make_int2(a.cell_seq[slot], a.cell_pos[slot]);
+        };
+        int2 nxt_cell = cell_of(w.kb_b);
         uint4 *orow = reinterpret_cast<uint4 *>(a.out + ((size_t)tok * a.Hq + h) * D);
         const int nseg = w.kb_e - w.kb_b;
         float m_run = -INFINITY, l_run = 0.f;
@@ -515,10 +535,20 @@ k_prefill(AttnArgs a, const __grid_constant__ AttnMaps maps) {
                                              (size_t)kPartStride * 128,
                                  kPartStride * 128 * 4);
           }
+          const int2 my_cell = nxt_cell;
+          if (MASK && kk + 1 < nseg) nxt_cell = cell_of(kb + 1);  // loads in flight meanwhile
           if (!pf_wait(&bars->s_full[wg], (sc + kk) & 1u, err, abort)) { ok = false; break; }
           tc::fence_after_sync();
           const int nv = min(max(L - kb * KB, 0), KB);  // valid keys of this row here
-          const bool wfull = __all_sync(0xffffffffu, nv == KB);
+          const bool wfull = !MASK && __all_sync(0xffffffffu, nv == KB);
+          const int2 *cb = reinterpret_cast<const int2 *>(smem + Cfg::kCinfo) +
+                           (wg * 2 + ((sc + kk) & 1u)) * 128;
+          if (MASK) {
+            // every thread of the warpgroup publishes its key's cell, then reads all 128
+            // (two buffers: a buffer is rewritten two blocks later, after the next sync)
+            const_cast<int2 *>(cb)[row] = my_cell;
+            asm volatile("bar.sync %0, 128;" ::"r"(1 + wg) : "memory");
+          }
           // The whole 128-column score row in one TMEM round trip (the tensor core keeps
           // TMEM busy, so each round trip costs hundreds of cycles).  Row max of the raw
           // scores over the valid keys (scale > 0 commutes with max); masked scores become
@@ -529,7 +559,24 @@ k_prefill(AttnArgs a, const __grid_constant__ AttnMaps maps) {
           tc::ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(t + 64));
           tc::ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(t + 96));
           tc::wait_ld();
-          if (!wfull) {
+          if (MASK) {
+            // the kept keys as a 128-bit mask first (a rolled loop over the cells keeps
+            // few registers live beside the score row), then applied to the scores
+            uint32_t mw[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint32_t m = 0;
+#pragma unroll 4
+              for (int b = 0; b < 32; ++b) {
+                const int2 ce = cb[q * 32 + b];
+                m |= (q * 32 + b < nv && ce.x == my_seq && ce.y <= my_pos) ? 1u << b : 0u;
+              }
+              mw[q] = m;
+            }
+#pragma unroll
+            for (int j = 0; j < 128; ++j)
+              t[j] = (mw[j >> 5] >> (j & 31)) & 1u ? t[j] : 0xff800000u;
+          } else if (!wfull) {
 #pragma unroll
             for (int j = 0; j < 128; ++j) t[j] = j < nv ? t[j] : 0xff800000u;  // -inf
           }
@@ -579,6 +626,22 @@ k_prefill(AttnArgs a, const __grid_constant__ AttnMaps maps) {
               for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
               tc::st32(tO + c * 32, o);
             }
+          }
+          if (MASK && wg == 0) {
+            // free cells may hold NaN: their V rows are zeroed before this block's PV
+            // products (the other tile's issuer runs its PV only after tile 0's turn)
+            const uint32_t cur = sc + kk;
+            const int st = cur % kPfStages;
+            if (!pf_wait(&bars->v_full[st], (cur / kPfStages) & 1u, err, abort)) { ok = false; break; }
+            if (my_cell.x < 0) {
+              for (int hf = 0; hf < Cfg::kHalves; ++hf) {
+                uint4 *vrow = reinterpret_cast<uint4 *>(smem + Cfg::kV + st * Cfg::kTile +
+                                                        hf * kBoxBytes + row * 128);
+#pragma unroll
+                for (int x = 0; x < 8; ++x) vrow[x] = make_uint4(0, 0, 0, 0);
+              }
+            }
+            fence_proxy_async();
           }
           tc::wait_st();
           tc::fence_before_sync();
@@ -725,7 +788,7 @@ k_prefill(AttnArgs a, const __grid_constant__ AttnMaps maps) {
   }
 }
 
-template <int D>
+template <int D, bool MASK>
 static cudaError_t launch_prefill_t(const AttnArgs &a, int num_sms, const AttnMaps *maps,
                                     cudaStream_t s) {
   using Cfg = PfCfg<D>;
@@ -734,21 +797,24 @@ static cudaError_t launch_prefill_t(const AttnArgs &a, int num_sms, const AttnMa
     // setmaxnreg.inc can only draw on registers the block was launched with: refuse to
     // launch (rather than wait forever) if the compiled allocation does not cover the split
     cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, k_prefill<D>);
+    cudaError_t e = cudaFuncGetAttributes(&fa, k_prefill<D, MASK>);
     if (e != cudaSuccess) return e;
     if (fa.numRegs * kPfThreads < kRegsSplitTotal) return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(k_prefill<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+    e = cudaFuncSetAttribute(k_prefill<D, MASK>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
     if (e != cudaSuccess) return e;
     setup.mark();
   }
-  k_prefill<D><<<num_sms, kPfThreads, Cfg::kSmem, s>>>(a, *maps);
+  k_prefill<D, MASK><<<num_sms, kPfThreads, Cfg::kSmem, s>>>(a, *maps);
   return cudaGetLastError();
 }
 
 cudaError_t launch_prefill(const AttnArgs &a, int num_sms, const void *tmaps, cudaStream_t s) {
   const AttnMaps *maps = static_cast<const AttnMaps *>(tmaps);
-  if (a.D == 128) return launch_prefill_t<128>(a, num_sms, maps, s);
-  if (a.D == 64) return launch_prefill_t<64>(a, num_sms, maps, s);
+  const bool mask = a.cell_seq != nullptr;
+  if (a.D == 128) return mask ? launch_prefill_t<128, true>(a, num_sms, maps, s)
+                              : launch_prefill_t<128, false>(a, num_sms, maps, s);
+  if (a.D == 64) return mask ? launch_prefill_t<64, true>(a, num_sms, maps, s)
+                             : launch_prefill_t<64, false>(a, num_sms, maps, s);
   return cudaErrorInvalidValue;
 }
 

@@ -2,7 +2,8 @@
 cache is one span of cells shared by every sequence; attention reads the whole
 span under a mask).  The oracle's masked attention is pinned to the paged
 definition (the mask keeps exactly a token's own cells) and to a numpy brute
-force; on the GPU the masked decode kernel is checked against it."""
+force; on the GPU the masked decode kernel (split-KV) and the masked prefill
+kernel (tcgen05 tiles) are checked against it."""
 import numpy as np
 import pytest
 
@@ -100,16 +101,21 @@ def pa():
     return m
 
 
-def run_masked(pa, case, kp, vp):
+def run_masked(pa, case, kp, vp, kind="decode", view=None):
+    """The masked kernel of `kind` (decode: split-KV, prefill: tcgen05 tiles) on the
+    span view of the case (or on the given tables)."""
     import torch
-    tpt, kv, cs, cp, ts, tp = workloads.span_view(case)
+    tpt, kv, cs, cp, ts, tp = workloads.span_view(case) if view is None else view
     dev = "cuda"
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
-    out = torch.empty((case.T, case.Hq, case.d), dtype=torch.float16, device=dev)
-    ws = pa.new_workspace(case.T, case.Hq, case.Hkv, case.d, dev)
-    pa.plan_decode(t(tpt), t(kv), case.Hq, case.Hkv, case.P, case.d, ws)
-    pa.masked_decode(t(case.q.view(np.float16)), t(kp.view(np.float16)), t(vp.view(np.float16)),
-                     t(tpt), t(kv), case.scale, t(cs), t(cp), t(ts), t(tp), out, ws)
+    T = tpt.shape[0]
+    out = torch.full((T, case.Hq, case.d), float("nan"), dtype=torch.float16, device=dev)
+    ws = pa.new_workspace(T, case.Hq, case.Hkv, case.d, dev)
+    plan = pa.plan_decode if kind == "decode" else pa.plan_prefill
+    run = pa.masked_decode if kind == "decode" else pa.masked_prefill
+    plan(t(tpt), t(kv), case.Hq, case.Hkv, case.P, case.d, ws)
+    run(t(case.q.view(np.float16)), t(kp.view(np.float16)), t(vp.view(np.float16)),
+        t(tpt), t(kv), case.scale, t(cs), t(cp), t(ts), t(tp), out, ws)
     torch.cuda.synchronize()
     assert pa.read_error(ws) == 0
     return out.float().cpu().numpy(), (tpt, kv, cs, cp, ts, tp)
@@ -153,3 +159,82 @@ def test_masked_decode_padding_token_gets_zero_row(pa):
     mref = oracle.masked_attention(case.q, kp, vp, tpt, kv, case.scale, cs, cp, ts, tp)
     from tests._gpu import assert_attn_close
     assert_attn_close(got, mref, "masked with padding")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("make", [
+    workloads.tiny, workloads.decode,
+    lambda s: workloads.small_prefill(s, P=128, d=128, Hq=8, Hkv=2),
+    lambda s: workloads.small_prefill(s, P=16, d=64, Hq=4, Hkv=2),
+    lambda s: workloads.small_prefill(s, P=64, d=128, Hq=4, Hkv=4)],
+    ids=["tiny", "decode", "prefill_P128_d128", "prefill_P16_d64", "prefill_G1"])
+def test_masked_prefill_matches_oracle(pa, make):
+    """The unified-span baseline on the tcgen05 tiles: tiles of 128 consecutive tokens of
+    any sequences, each streaming the whole span (free cells hold NaN)."""
+    from tests._gpu import assert_attn_close
+    case = make(0)
+    ref, kp, vp = paged_ref(case)
+    got, (tpt, kv, cs, cp, ts, tp) = run_masked(pa, case, kp, vp, kind="prefill")
+    mref = oracle.masked_attention(case.q, kp, vp, tpt, kv, case.scale, cs, cp, ts, tp)
+    assert_attn_close(got, mref, f"masked prefill {case.name}")
+    assert_attn_close(got, ref, f"masked prefill vs paged {case.name}")
+
+
+@pytest.mark.gpu
+def test_masked_prefill_random_cells(pa):
+    """Random cell owners and positions (three sequences, free cells holding NaN), random
+    rows and lengths: against the oracle and the numpy brute force."""
+    from tests._gpu import assert_attn_close
+    rng = np.random.default_rng(12)
+    N, Hkv, P, d, Hq, T = 24, 2, 16, 64, 4, 150
+    case = workloads.tiny(0)
+    case.Hq, case.Hkv, case.P, case.d, case.scale = Hq, Hkv, P, d, 0.125
+    kp = workloads.randn_f16(rng, (N, Hkv, P, d))
+    vp = workloads.randn_f16(rng, (N, Hkv, P, d))
+    case.q = workloads.randn_f16(rng, (T, Hq, d))
+    cs = rng.integers(-1, 3, N * P).astype(np.int32)
+    cp = rng.integers(0, 300, N * P).astype(np.int32)
+    free = np.flatnonzero(cs < 0)
+    kp[free // P, :, free % P, :] = 0x7E00
+    vp[free // P, :, free % P, :] = 0x7E00
+    ts = rng.integers(0, 3, T).astype(np.int32)
+    tp = rng.integers(100, 300, T).astype(np.int32)
+    row = rng.permutation(N).astype(np.int32)
+    tpt = np.tile(row, (T, 1))        # one row for all: tiles of 128 mixed tokens
+    kv = np.full(T, N * P, np.int32)
+    kv[:7] = rng.integers(1, N * P, 7)  # ...and a few short ones
+    got, _ = run_masked(pa, case, kp, vp, kind="prefill", view=(tpt, kv, cs, cp, ts, tp))
+    mref = oracle.masked_attention(case.q, kp, vp, tpt, kv, case.scale, cs, cp, ts, tp)
+    assert_attn_close(got, mref, "masked prefill, random cells")
+    assert_attn_close(got, brute_masked(case.q, kp, vp, tpt, kv, case.scale, cs, cp, ts, tp),
+                      "masked prefill vs brute force")
+
+
+@pytest.mark.gpu
+def test_masked_prefill_8x16k_ubatch_sampled(pa):
+    """One late ubatch of the 8 x 16K schedule over the span of the whole 1280-page pool:
+    every tile streams the pool (the baseline the page's TTFT claim is measured against)."""
+    from tests._gpu import assert_attn_close
+    wl = workloads.Prefill8x16K(0)
+    u = 40
+    ts, tp, q, _, _ = wl.ubatch(u)
+    kf, vf = wl.pool_final()
+    N, P = wl.num_pages, wl.P
+    cs = np.full(N * P, -1, np.int32)
+    cp = np.full(N * P, -1, np.int32)
+    for s_ in range(wl.n_seq):
+        pos = np.arange(wl.seq_len)
+        slots = wl.seq_page_table[s_][pos // P].astype(np.int64) * P + pos % P
+        cs[slots], cp[slots] = s_, pos
+    T = ts.shape[0]
+    tpt = np.tile(np.arange(N, dtype=np.int32), (T, 1))
+    kv = np.full(T, N * P, np.int32)
+
+    class C:  # the shape fields run_masked reads
+        Hq, Hkv, d, scale = wl.Hq, wl.Hkv, wl.d, wl.scale
+    C.P, C.q = P, q
+    got, _ = run_masked(pa, C, kf, vf, kind="prefill", view=(tpt, kv, cs, cp, ts, tp))
+    sel = np.array([0, 127, 128, 700, 1300, T - 1], np.int32)
+    tpt_p, kv_p, _ = oracle.expand_ubatch(wl.seq_page_table, ts, tp, P)
+    ref = oracle.paged_attention(q, kf, vf, tpt_p, kv_p, wl.scale, tokens=sel)
+    assert_attn_close(got[sel], ref, "masked prefill 8x16K ubatch vs paged oracle")
