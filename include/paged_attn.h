@@ -18,7 +18,8 @@
  *              paged_attn_forward, paged_attn_forward_noalloc
  *  around it:  paged_attn_workspace_size, paged_attn_validate,
  *              paged_attn_read_error, paged_attn_strerror, paged_attn_version,
- *              paged_attn_set_prefill_min_run, pa_pool_* (host page pool)
+ *              paged_attn_set_prefill_min_run, paged_attn_set_decode_wait_limit,
+ *              pa_pool_* (host page pool)
  *  beyond it:  paged_attn_plan_decode, paged_attn_plan_prefill;
  *              paged_attn_masked_decode and paged_attn_masked_prefill (the
  *              unified-span baseline that paging replaces); paged_kv_append_fp8
@@ -355,6 +356,21 @@ int paged_attn_read_error(const void *workspace, int *err_host, void *stream);
  * plans made after the call.  Returns the previous value.
  */
 int paged_attn_set_prefill_min_run(int min_run);
+
+/*
+ * Limit, in nanoseconds, of every bounded device-side wait of the split-KV decode
+ * kernel (paged_attn_decode, paged_attn_masked_decode, paged_attn_decode_fp8 and the
+ * decode part of paged_attn_run / _forward); default 2 s.  0 restores the default;
+ * values below 1000 become 1000.  Process-wide; affects launches made after the call.
+ * Returns the previous value.  A wait that gives up sets PA_ERR_TIMEOUT in the
+ * workspace error word; every role of the CTA then stops, the copies it already
+ * issued land (their own, unshortened bound) and the launch returns with the rows it
+ * did not finish unwritten.  After such a launch, plan again before the next run (the
+ * plan's arrival counters may be left mid-count).  The other kernels keep the fixed
+ * 2 s limit.  Meant for tests of the timeout path and for callers that prefer an
+ * early error to a long stall.
+ */
+unsigned long long paged_attn_set_decode_wait_limit(unsigned long long ns);
 
 /*
  * Host-side page pool (the per-sequence page mapping of 作品简介; CacheFlow

@@ -56,6 +56,7 @@ _SIGS = {
     "paged_attn_validate": ([_vp, _i, _vp, _i, _i, _i, _vp, _vp], _i),
     "paged_attn_read_error": ([_vp, ctypes.POINTER(_i), _vp], _i),
     "paged_attn_set_prefill_min_run": ([_i], _i),
+    "paged_attn_set_decode_wait_limit": ([ctypes.c_ulonglong], ctypes.c_ulonglong),
     "pa_pool_create": ([_i], _vp),
     "pa_pool_destroy": ([_vp], None),
     "pa_pool_num_free": ([_vp], _i),
@@ -340,6 +341,12 @@ def read_error(workspace, stream=None) -> int:
     if st not in (PA_OK, PA_EDEVICE):
         raise PagedAttnError(st, "paged_attn_read_error")
     return int(v.value)
+
+
+def set_decode_wait_limit(ns: int) -> int:
+    """Limit (ns) of the split-KV decode kernel's bounded waits (0: the 2 s default).
+    Returns the previous value."""
+    return int(_lib.paged_attn_set_decode_wait_limit(int(ns)))
 
 
 def set_prefill_min_run(n: int) -> int:

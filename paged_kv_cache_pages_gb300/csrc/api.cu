@@ -24,6 +24,7 @@ struct NvtxRange {
 };
 
 std::atomic<int> g_min_run{16};
+std::atomic<unsigned long long> g_decode_wait_ns{kWaitLimitNs};
 
 int sm_count() {
   int dev = 0;
@@ -99,6 +100,7 @@ AttnArgs make_args(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v
   a.scale_log2 = scale * kLog2e;
   a.cell_seq = a.cell_pos = a.tok_seq = a.tok_pos = nullptr;
   a.k_scale = a.v_scale = nullptr;
+  a.wait_ns = g_decode_wait_ns.load();
   return a;
 }
 
@@ -409,6 +411,12 @@ int paged_attn_read_error(const void *workspace, int *err_host, void *stream) {
   if (cudaStreamSynchronize(s) != cudaSuccess) return PA_ELAUNCH;
   *err_host = v;
   return v == 0 ? PA_OK : PA_EDEVICE;
+}
+
+unsigned long long paged_attn_set_decode_wait_limit(unsigned long long ns) {
+  if (ns == 0) ns = kWaitLimitNs;
+  if (ns < 1000ull) ns = 1000ull;
+  return g_decode_wait_ns.exchange(ns);
 }
 
 int paged_attn_set_prefill_min_run(int min_run) {

@@ -136,8 +136,12 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 }
 
 // Bounded wait on an mbarrier phase.  Returns false (and sets PA_ERR_TIMEOUT in
-// *err) if the phase did not complete within ~2 s of wall time.
+// *err) if the phase did not complete within ~2 s of wall time.  (The split-KV decode
+// kernel takes its limit from the host, default the same 2 s.)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+// Bound of the waits that let a kernel's own copies in flight land before it exits
+// (never shortened: the copies must land).
+constexpr uint64_t kDrainLimitNs = 2000000000ull;
 
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *err) {
   if (mbar_try_wait(bar, parity)) return true;

@@ -103,6 +103,9 @@ struct DecBars {
   uint64_t fetched;  // the combining warp answered the fetch of the final segment's parts
   StageMeta meta[6];
   int abort;
+  int issued;     // stages the producer has issued (consumers' view after an abort)
+  int prod_done;  // 1: the producer issues no more stages
+  int fetch_go;   // the outcome of the consumers' wait for the fetch, one for all
   int last;     // the consumers complete the split of the CTA's final segment
   int fetch_ok; // 1: every other part of the final segment sits in the fetch area
   int tail;     // the consumers reached the end of the final segment
@@ -171,18 +174,47 @@ __device__ __forceinline__ void it_next(UnitIt &it, const DecView &v) {
   it.i = v.n_dec;  // past the end (never consumed)
 }
 
-// Bounded wait that also gives up as soon as another thread of the CTA gave up.
+// Bounded wait (limit in ns) that also gives up as soon as another thread of the CTA
+// gave up.
 __device__ __forceinline__ bool dec_wait(uint64_t *bar, uint32_t parity, int *err,
-                                         volatile int *abort) {
+                                         volatile int *abort, uint64_t limit) {
   if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 0;; ++it) {
+  for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if ((it & 127u) == 127u && globaltimer_ns() - t0 > kWaitLimitNs) {
+    // each try_wait may suspend the thread for a while: the clock is read every time
+    if (globaltimer_ns() - t0 > limit) {
       atomicOr(err, PA_ERR_TIMEOUT);
       *abort = 1;
       return false;
+    }
+  }
+}
+
+// The consumers' wait for stage k.  Every consumer warp must reach the same verdict,
+// since they meet at named barriers afterwards: once the CTA gives up, stage k is still
+// consumed if the producer had issued it (its copies land; wait for them), and
+// abandoned only when the producer has stopped short of it.  The last-resort bound,
+// twice the drain bound, is never reached while the producer's own waits are bounded.
+__device__ __forceinline__ bool dec_wait_stage(uint64_t *bar, uint32_t parity, int k, int *err,
+                                               volatile int *abort, volatile int *issued,
+                                               volatile int *prod_done, uint64_t limit) {
+  if (mbar_try_wait(bar, parity)) return true;
+  uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) {
+      if (*prod_done) {
+        __threadfence_block();
+        if (k >= *issued) return false;
+      }
+      if (globaltimer_ns() - t0 > 2 * kDrainLimitNs) return false;
+      continue;
+    }
+    if (globaltimer_ns() - t0 > limit) {
+      atomicOr(err, PA_ERR_TIMEOUT);
+      *abort = 1;
     }
   }
 }
@@ -333,6 +365,8 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
     }
     mbar_init(&bars->fetched, 1);
     bars->abort = 0;
+    bars->issued = 0;
+    bars->prod_done = 0;
     bars->fetch_ok = 0;
     bars->tail = 0;
     fence_mbar_init();
@@ -488,7 +522,7 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
       }
       for (int k = 0; k < n; ++k) {
         const int st = k % NS;
-        if (!dec_wait(&bars->empty[st], ((k / NS) & 1) ^ 1, err, abort)) break;
+        if (!dec_wait(&bars->empty[st], ((k / NS) & 1) ^ 1, err, abort, a.wait_ns)) break;
         unsigned char *stage = ring + st * Cfg::kStage;
         int rows = min(KB, pit.L - pit.kb * KB);
         // every page of the block must exist, else the block is skipped (and flagged)
@@ -561,15 +595,19 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
           bulk_g2s(stage + 2 * Cfg::kBlk, a.q + ((size_t)pit.tok * a.Hq + pit.g * G) * D, qbytes,
                    &bars->full[st]);
         ++issued;
+        *reinterpret_cast<volatile int *>(&bars->issued) = issued;
         it_next(pit, v);
         if (k + 1 < n) fetch_pages(pit);
       }
+      // no more stages: the consumers may stop waiting for any stage past `issued`
+      __threadfence_block();
+      *reinterpret_cast<volatile int *>(&bars->prod_done) = 1;
       // after giving up, let copies already in flight land before the CTA exits
       if (*abort) {
         for (int k = issued - NS > 0 ? issued - NS : 0; k < issued; ++k) {
           uint64_t t0 = globaltimer_ns();
           while (!mbar_try_wait(&bars->full[k % NS], (k / NS) & 1) &&
-                 globaltimer_ns() - t0 < kWaitLimitNs) {
+                 globaltimer_ns() - t0 < kDrainLimitNs) {
           }
         }
       }
@@ -584,7 +622,7 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
       volatile int *tail = &bars->tail;
       for (int j = 0;; ++j) {
         const int q = j % kJobs;
-        if (!dec_wait(&bars->job_full[q], (j / kJobs) & 1, err, abort)) break;
+        if (!dec_wait(&bars->job_full[q], (j / kJobs) & 1, err, abort, a.wait_ns)) break;
         const DecJob job = bars->jobs[q];
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->job_empty[q]);
@@ -606,7 +644,7 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
                 ok = 1;
                 break;
               }
-              if (*tail || *abort || globaltimer_ns() - t0 > kWaitLimitNs) break;
+              if (*tail || *abort || globaltimer_ns() - t0 > a.wait_ns) break;
               __nanosleep(128);
             }
           }
@@ -719,7 +757,9 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
     unsigned char *stage = ring + st * Cfg::kStage;
     const uint32_t sK = smem_u32(stage), sV = smem_u32(stage + Cfg::kBlk);
     // every consumer warp sees the same outcome of this wait, so all leave together
-    if (!dec_wait(&bars->full[st], (k / NS) & 1, err, abort)) break;
+    if (!dec_wait_stage(&bars->full[st], (k / NS) & 1, k, err, abort, &bars->issued,
+                        &bars->prod_done, a.wait_ns))
+      break;
     const StageMeta cit = bars->meta[st];  // the unit this stage holds
     const int rows = cit.rows;
     const bool seg_first = (k == 0) || cit.kb == 0;
@@ -734,7 +774,7 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
         fin = seg_parts(seg_begin, seg_end, U, C);
         if (tid == 0) {
           const int q = n_jobs % kJobs;
-          if (dec_wait(&bars->job_empty[q], ((n_jobs / kJobs) & 1) ^ 1, err, abort)) {
+          if (dec_wait(&bars->job_empty[q], ((n_jobs / kJobs) & 1) ^ 1, err, abort, a.wait_ns)) {
             DecJob job;
             job.ig = cit.i * a.Hkv + cit.g;
             job.tok = cit.tok;
@@ -993,8 +1033,13 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
         // their parts long ago (the next CTA starts its range with it) and the combining
         // warp has already copied them here; then the row is finished from shared
         // memory.  Otherwise publish this part; the last to arrive combines.
-        if (tid == 0) *reinterpret_cast<volatile int *>(&bars->tail) = 1;
-        if (dec_wait(&bars->fetched, 0, err, abort)) {
+        if (tid == 0) {
+          *reinterpret_cast<volatile int *>(&bars->tail) = 1;
+          // one waiter decides for all the consumers, which meet at named barriers below
+          bars->fetch_go = dec_wait(&bars->fetched, 0, err, abort, a.wait_ns) ? 1 : 0;
+        }
+        consumers_sync();
+        if (*reinterpret_cast<volatile int *>(&bars->fetch_go)) {
           const bool fetched = *reinterpret_cast<volatile int *>(&bars->fetch_ok) != 0;
           bool combine = fetched;
           if (!fetched) {
@@ -1069,7 +1114,7 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
       } else if (!direct && tid == 0) {
         // hand the cross-CTA combine to the combining warp
         const int q = n_jobs % kJobs;
-        if (dec_wait(&bars->job_empty[q], ((n_jobs / kJobs) & 1) ^ 1, err, abort)) {
+        if (dec_wait(&bars->job_empty[q], ((n_jobs / kJobs) & 1) ^ 1, err, abort, a.wait_ns)) {
           const SegParts sp = seg_parts(seg_begin, seg_begin + seg_units, U, C);
           DecJob job;
           job.ig = ig;
@@ -1087,7 +1132,7 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
   }
   if (tid == 0) {  // no more jobs
     const int q = n_jobs % kJobs;
-    if (dec_wait(&bars->job_empty[q], ((n_jobs / kJobs) & 1) ^ 1, err, abort)) {
+    if (dec_wait(&bars->job_empty[q], ((n_jobs / kJobs) & 1) ^ 1, err, abort, a.wait_ns)) {
       bars->jobs[q].ig = -1;
       mbar_arrive(&bars->job_full[q]);
     }

@@ -59,6 +59,8 @@ struct AttnArgs {
   const int32_t *cell_seq, *cell_pos, *tok_seq, *tok_pos;
   // FP8 pages only, else null: the binary32 scale of every cached (page, head, row)
   const float *k_scale, *v_scale;
+  // bounded-wait limit of the split-KV decode kernel, in ns (paged_attn_set_decode_wait_limit)
+  unsigned long long wait_ns;
 };
 
 // Decode: split-KV over all SMs plus the log-sum-exp reduce.  Returns a

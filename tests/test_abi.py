@@ -138,3 +138,11 @@ def test_noalloc_host_checks_match_forward(pa):
         want = fwd(nul, nul, nul, nul, mp, nul, T, Hq, Hkv, P, d, npg, 0.1, nul, nul, 0, nul)
         got = noa(nul, nul, nul, nul, mp, nul, T, Hq, Hkv, P, d, npg, 0.1, nul, nul)
         assert got == want, ((mp, T, Hq, Hkv, P, d, npg), got, want)
+
+
+def test_decode_wait_limit_setter(pa):
+    default = pa.set_decode_wait_limit(5000)
+    assert default == 2_000_000_000
+    assert pa.set_decode_wait_limit(10) == 5000          # clamps to 1 us
+    assert pa.set_decode_wait_limit(0) == 1000           # 0 restores the default
+    assert pa.set_decode_wait_limit(default) == 2_000_000_000
