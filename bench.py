@@ -670,10 +670,11 @@ def bench_unified_span_prefill(pa, torch, pb, steps, warmup, world, paged_ms_per
                     "llama.cpp's unified cache reads the span the same way"}
 
 
-def bench_fp8_decode(pa, torch, db, steps, warmup, world, hbm, f16_ms_per_layer):
-    """FP8 KV pages on the decode workload: the same 36 layers with every cached row
+def bench_fp8_decode(pa, torch, db, steps, warmup, world, hbm, f16_ms_per_layer,
+                     workload="decode_8seq_fp8_pages", traffic_key="k_decode_fp8"):
+    """FP8 KV pages on a decode workload: the same layers with every cached row
     quantised (E4M3 codes, one scale per row) by the library's quantising append;
-    one plan, then 36 FP8 decode launches back to back."""
+    one plan, then the FP8 decode launches back to back."""
     c = db.case
     dev = db.q[0].device
     rows_k, rows_v, slots = [], [], []
@@ -704,14 +705,14 @@ def bench_fp8_decode(pa, torch, db, steps, warmup, world, hbm, f16_ms_per_layer)
         raise RuntimeError("device error word set in the FP8 decode")
     nbytes = float(c.seq_len.astype(np.int64).sum()) * c.Hkv * (2 * c.d + 2 * 4)
     gbs = nbytes / (ms_layer / 1e3) / 1e9
-    return {"workload": "decode_8seq_fp8_pages", "unit": "GB/s", "value": round(gbs * world, 1),
+    return {"workload": workload, "unit": "GB/s", "value": round(gbs * world, 1),
             "ms_per_layer": round(ms_layer, 4), "bytes_per_layer": nbytes,
             "f16_ms_per_layer": round(f16_ms_per_layer, 4),
             "speedup_vs_f16": round(f16_ms_per_layer / ms_layer, 2),
             "roofline": {"bound": "hbm", "kernel": "k_decode (FP8 pages)",
                          "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
-                         "frac": round(gbs / hbm, 4), "traffic": traffic_of("k_decode_fp8")},
-            "timing": "CUDA graph of one plan and 36 FP8 decode launches (one per layer)"}
+                         "frac": round(gbs / hbm, 4), "traffic": traffic_of(traffic_key)},
+            "timing": f"CUDA graph of one plan and {db.layers} FP8 decode launches (one per layer)"}
 
 
 LONGTAIL_LAYERS = 4
@@ -748,6 +749,10 @@ def bench_longtail(pa, torch, dev, steps, warmup, world, hbm, with_cpu, seed=0):
                                   "back (appends left out)",
                         "traffic": traffic_of("k_decode_longtail")},
            "timing": "value: CUDA graph of expansion, plan and 4 x (append + decode)"}
+    # FP8 pages on the same long-tail layer: half the bytes, where streaming dominates
+    res["fp8_pages"] = bench_fp8_decode(pa, torch, db, steps, warmup, world, hbm, t_kern * 1e3,
+                                        workload="decode_longtail_64seq_fp8_pages",
+                                        traffic_key="k_decode_fp8_longtail")
     if with_cpu:
         res["cpu_baseline"] = cpu_baseline_decode(c, reps_budget_s=3.0)
         res["cpu_baseline"]["sample"] = res["cpu_baseline"]["sample"].replace(

@@ -9,6 +9,10 @@
       copies of the 82 MB pool used in turn (default 8: 660 MB, larger than L2,
       so every call streams its pool from HBM).
 
+  python -m paged_kv_cache_pages_gb300.profile_case longtail [--reps R] [--pools N]
+      the long-tail decode layer (64 sequences, lognormal lengths, 1.06 GB of K/V):
+      expand -> plan -> append -> decode over N pool copies in turn (use 2: 3 GB).
+
   python -m paged_kv_cache_pages_gb300.profile_case span [--reps R]
       the unified-span baseline on the decode layer: every token reads the whole
       pool under a per-cell mask (one plan + masked decode per call).
@@ -76,8 +80,8 @@ def prefill(ubatch: int, reps: int):
           f"{flops / ms / 1e9:.1f} TFLOP/s (prefill+decode calls)")
 
 
-def decode(reps: int, n_pools: int):
-    c = workloads.decode(0)
+def decode(reps: int, n_pools: int, longtail: bool = False):
+    c = workloads.longtail(0) if longtail else workloads.decode(0)
     dev = "cuda"
     spt = torch.from_numpy(c.seq_page_table()).to(dev)
     kp = torch.from_numpy(c.k_pool.view(np.float16)).to(dev)
@@ -102,7 +106,7 @@ def decode(reps: int, n_pools: int):
     if pa.read_error(ws):
         raise SystemExit("device error word set")
     nbytes = float(c.seq_len.astype(np.int64).sum()) * c.Hkv * c.d * 4
-    print(f"decode: {ms * 1e3:.1f} us/call {nbytes / ms / 1e6:.1f} GB/s "
+    print(f"{c.name}: {ms * 1e3:.1f} us/call {nbytes / ms / 1e6:.1f} GB/s "
           f"({len(pools)} pools in turn, eager launches)")
 
 
@@ -183,7 +187,7 @@ def copy(reps: int):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["prefill", "decode", "copy", "span", "fp8"])
+    ap.add_argument("case", choices=["prefill", "decode", "longtail", "copy", "span", "fp8"])
     ap.add_argument("--ubatch", type=int, default=48)
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--pools", type=int, default=8)
@@ -192,6 +196,8 @@ def main():
         prefill(a.ubatch, a.reps)
     elif a.case == "decode":
         decode(a.reps, a.pools)
+    elif a.case == "longtail":
+        decode(a.reps, a.pools, longtail=True)
     elif a.case == "span":
         span(a.reps)
     elif a.case == "fp8":
