@@ -14,8 +14,8 @@
  * Entry points
  * ------------
  *  the path:   paged_expand_ubatch, paged_kv_append, paged_attn_plan,
- *              paged_attn_prefill, paged_attn_decode, paged_attn_run,
- *              paged_attn_forward, paged_attn_forward_noalloc
+ *              paged_attn_prefill, paged_attn_decode, paged_attn_decode_append,
+ *              paged_attn_run, paged_attn_forward, paged_attn_forward_noalloc
  *  around it:  paged_attn_workspace_size, paged_attn_validate,
  *              paged_attn_read_error, paged_attn_strerror, paged_attn_version,
  *              paged_attn_set_prefill_min_run, paged_attn_set_decode_wait_limit,
@@ -169,6 +169,27 @@ int paged_attn_decode(const uint16_t *q, const uint16_t *k_pages, const uint16_t
                       const int32_t *tok_page_table, int max_pages, const int32_t *tok_kv_len,
                       int T, int Hq, int Hkv, int P, int d, int num_pages, float scale,
                       uint16_t *out, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * paged_attn_decode with the decode step's append fused in: the launch also writes
+ * the new K and V rows of the planned decode tokens (reshape-and-cache, CacheFlow
+ * page, section 核心架构 3), so a decode layer is one launch instead of two.
+ *   k_new, v_new [T][Hkv][d] binary16 (16-byte aligned); slot_mapping [T] int64, as
+ *   paged_kv_append; k_pages, v_pages are written.  Other arguments as
+ *   paged_attn_decode (a preceding plan on the same workspace).
+ * Each decode token's new row must be its last key (slot of position kv_len - 1), as
+ * in a decode step, and a sequence may have at most one decode token in the ubatch:
+ * the row is written by the CTA that reads it, just before it reads it.  A token with
+ * slot < 0 is not written; a slot other than its last key's sets PA_ERR_SLOT_RANGE and
+ * is not written.  Rows of tokens on the prefill path are not written (append them
+ * with paged_kv_append).  The result equals paged_kv_append then paged_attn_decode.
+ */
+int paged_attn_decode_append(const uint16_t *q, const uint16_t *k_new, const uint16_t *v_new,
+                             const int64_t *slot_mapping, uint16_t *k_pages, uint16_t *v_pages,
+                             const int32_t *tok_page_table, int max_pages,
+                             const int32_t *tok_kv_len, int T, int Hq, int Hkv, int P, int d,
+                             int num_pages, float scale, uint16_t *out, void *workspace,
+                             size_t workspace_bytes, void *stream);
 
 /* paged_attn_prefill followed by paged_attn_decode (a planned ubatch). */
 int paged_attn_run(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,

@@ -73,6 +73,8 @@ _SIGS = {
     "paged_attn_plan_decode": ([_vp, _i, _vp, _i, _i, _i, _i, _i, _vp, _sz, _vp], _i),
     "paged_attn_masked_decode": ([_vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i,
                                   ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i),
+    "paged_attn_decode_append": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i,
+                                  _i, ctypes.c_float, _vp, _vp, _sz, _vp], _i),
     "paged_attn_plan_prefill": ([_vp, _i, _vp, _i, _i, _i, _i, _i, _vp, _sz, _vp], _i),
     "paged_attn_masked_prefill": ([_vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i,
                                    ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i),
@@ -326,6 +328,26 @@ def prefill(q, k_pages, v_pages, tok_page_table, tok_kv_len, scale, out, workspa
 def decode(q, k_pages, v_pages, tok_page_table, tok_kv_len, scale, out, workspace, stream=None):
     return _attn("paged_attn_decode", q, k_pages, v_pages, tok_page_table, tok_kv_len, scale, out,
                  workspace, stream)
+
+
+def decode_append(q, k_new, v_new, slot_mapping, k_pages, v_pages, tok_page_table, tok_kv_len,
+                  scale, out, workspace, stream=None):
+    """decode with the decode tokens' K/V append fused into the same launch (f16 pages):
+    equals kv_append(k_new, v_new, slot_mapping, ...) then decode(...)."""
+    for t, n in ((q, "q"), (k_new, "k_new"), (v_new, "v_new"), (k_pages, "k_pages"),
+                 (v_pages, "v_pages"), (out, "out")):
+        _req(t, torch.float16, n)
+    _req(slot_mapping, torch.int64, "slot_mapping")
+    _req(tok_page_table, torch.int32, "tok_page_table")
+    _req(tok_kv_len, torch.int32, "tok_kv_len")
+    T, Hq, d = q.shape
+    N, Hkv, P, _ = k_pages.shape
+    _check(_lib.paged_attn_decode_append(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(k_pages), _ptr(v_pages),
+        _ptr(tok_page_table), tok_page_table.shape[1], _ptr(tok_kv_len), T, Hq, Hkv, P, d, N,
+        float(scale), _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)),
+        "paged_attn_decode_append")
+    return out
 
 
 def validate(tok_page_table, tok_kv_len, P, num_pages, err, stream=None):

@@ -101,6 +101,8 @@ AttnArgs make_args(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v
   a.cell_seq = a.cell_pos = a.tok_seq = a.tok_pos = nullptr;
   a.k_scale = a.v_scale = nullptr;
   a.wait_ns = g_decode_wait_ns.load();
+  a.k_new = a.v_new = nullptr;
+  a.slot = nullptr;
   return a;
 }
 
@@ -356,6 +358,29 @@ int paged_attn_decode(const uint16_t *q, const uint16_t *k_pages, const uint16_t
   if (st != PA_OK || T == 0) return st;
   AttnArgs a = make_args(q, k_pages, v_pages, tok_page_table, max_pages, tok_kv_len, T, Hq, Hkv, P,
                          d, num_pages, scale, out, workspace);
+  AttnMaps maps;
+  st = encode_attn_maps(a, &maps);
+  if (st != PA_OK) return st;
+  return launch_status(launch_decode(a, sm_count(), &maps, static_cast<cudaStream_t>(stream)));
+}
+
+int paged_attn_decode_append(const uint16_t *q, const uint16_t *k_new, const uint16_t *v_new,
+                             const int64_t *slot_mapping, uint16_t *k_pages, uint16_t *v_pages,
+                             const int32_t *tok_page_table, int max_pages,
+                             const int32_t *tok_kv_len, int T, int Hq, int Hkv, int P, int d,
+                             int num_pages, float scale, uint16_t *out, void *workspace,
+                             size_t workspace_bytes, void *stream) {
+  NvtxRange nvtx_range("paged_attn_decode_append");
+  int st = check_attn(q, k_pages, v_pages, tok_page_table, max_pages, tok_kv_len, T, Hq, Hkv, P, d,
+                      num_pages, out, workspace, workspace_bytes, true);
+  if (st != PA_OK || T == 0) return st;
+  if (!k_new || !v_new || !slot_mapping) return PA_EINVAL;
+  if (!aligned16(k_new) || !aligned16(v_new)) return PA_EALIGN;
+  AttnArgs a = make_args(q, k_pages, v_pages, tok_page_table, max_pages, tok_kv_len, T, Hq, Hkv, P,
+                         d, num_pages, scale, out, workspace);
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.slot = slot_mapping;
   AttnMaps maps;
   st = encode_attn_maps(a, &maps);
   if (st != PA_OK) return st;

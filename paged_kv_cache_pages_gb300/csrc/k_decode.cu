@@ -101,6 +101,7 @@ struct DecBars {
   uint64_t job_full[kJobs], job_empty[kJobs];
   DecJob jobs[kJobs];
   uint64_t fetched;  // the combining warp answered the fetch of the final segment's parts
+  int append_upto;   // fused append: the new rows of this CTA's units < append_upto are in the pool
   StageMeta meta[6];
   int abort;
   int issued;     // stages the producer has issued (consumers' view after an abort)
@@ -180,11 +181,11 @@ __device__ __forceinline__ bool dec_wait(uint64_t *bar, uint32_t parity, int *er
                                          volatile int *abort, uint64_t limit) {
   if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 0;; ++it) {
+  for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    // each try_wait may suspend the thread for a while: the clock is read every 8th
-    if ((it & 7u) == 7u && globaltimer_ns() - t0 > limit) {
+    // each try_wait may suspend the thread for a while: the clock is read every time
+    if (globaltimer_ns() - t0 > limit) {
       atomicOr(err, PA_ERR_TIMEOUT);
       *abort = 1;
       return false;
@@ -202,17 +203,17 @@ __device__ __forceinline__ bool dec_wait_stage(uint64_t *bar, uint32_t parity, i
                                                volatile int *prod_done, uint64_t limit) {
   if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 0;; ++it) {
+  for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) {
       if (*prod_done) {
         __threadfence_block();
         if (k >= *issued) return false;
       }
-      if ((it & 7u) == 7u && globaltimer_ns() - t0 > 2 * kDrainLimitNs) return false;
+      if (globaltimer_ns() - t0 > 2 * kDrainLimitNs) return false;
       continue;
     }
-    if ((it & 7u) == 7u && globaltimer_ns() - t0 > limit) {
+    if (globaltimer_ns() - t0 > limit) {
       atomicOr(err, PA_ERR_TIMEOUT);
       *abort = 1;
     }
@@ -246,6 +247,15 @@ __device__ __forceinline__ int4 ld_v4_early(const int4 *p) {
 __device__ __forceinline__ int ld_acquire(const int *p) {
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// CTA-scope release/acquire on a shared-memory flag
+__device__ __forceinline__ void st_release_cta(int *p, int v) {
+  asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire_cta(const int *p) {
+  int v;
+  asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
   return v;
 }
 __device__ __forceinline__ int atom_add_acq_rel(int *p, int x) {
@@ -364,6 +374,7 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
       mbar_init(&bars->job_empty[j], 1);
     }
     mbar_init(&bars->fetched, 1);
+    bars->append_upto = 0;
     bars->abort = 0;
     bars->issued = 0;
     bars->prod_done = 0;
@@ -492,6 +503,7 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
   const int n = u1 - u0;
 
   volatile int *abort = &bars->abort;
+  const bool appending = !KV8 && !MASK && a.k_new != nullptr;
 
   if (w >= kDecWarps) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kDecRegsOther));
@@ -520,9 +532,27 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
         pgs[0] = p0.x; pgs[1] = p0.y; pgs[2] = p0.z; pgs[3] = p0.w;
         pgs[4] = p1.x; pgs[5] = p1.y; pgs[6] = p1.z; pgs[7] = p1.w;
       }
+      int appended = appending ? 0 : n;  // units whose new rows are known to be written
       for (int k = 0; k < n; ++k) {
         const int st = k % NS;
         if (!dec_wait(&bars->empty[st], ((k / NS) & 1) ^ 1, err, abort, a.wait_ns)) break;
+        // fused append: a token's last key block holds its new row, which this CTA's
+        // append warp writes (in unit order, publishing how far it got); read the block
+        // only once its row is written
+        if (appended <= k && pit.kb + 1 == pit.units) {
+          uint64_t t0 = 0;
+          while ((appended = ld_acquire_cta(&bars->append_upto)) <= k) {
+            if (*abort) break;
+            if (t0 == 0) {
+              t0 = globaltimer_ns();
+            } else if (globaltimer_ns() - t0 > a.wait_ns) {
+              atomicOr(err, PA_ERR_TIMEOUT);
+              *abort = 1;
+              break;
+            }
+          }
+          if (appended <= k) break;
+        }
         unsigned char *stage = ring + st * Cfg::kStage;
         int rows = min(KB, pit.L - pit.kb * KB);
         // every page of the block must exist, else the block is skipped (and flagged)
@@ -611,6 +641,80 @@ k_decode(AttnArgs a, const __grid_constant__ AttnMaps maps) {
           }
         }
       }
+    } else if (w == kDecWarps + 2 && appending) {
+      // -------------------------------------------------------------- fused append
+      // The new K/V row of each decode token is its last key (position kv_len - 1),
+      // in the last key block of each (token, head), and only the CTA owning that unit
+      // reads it: this warp writes the rows of this CTA's such units (a row of one
+      // head is D / 8 16-byte chunks of K, then as many of V, one lane each), then
+      // releases the producer.  A slot other than the last key's is flagged, not
+      // written.
+      // (token, head) segments are visited in unit order from the CTA's first; a
+      // segment's last unit is in this CTA's range [u0, u1) or not, without walking
+      // the units one by one.  The lanes load 32 tokens' records at once (a range of
+      // short sequences covers many tokens), then the warp walks them in order.
+      const int4 rec0 = reinterpret_cast<const int4 *>(a.ws + a.lay.dec_start)[4 * c];
+      uint16_t *kpw = const_cast<uint16_t *>(a.k_pages);
+      uint16_t *vpw = const_cast<uint16_t *>(a.v_pages);
+      constexpr int kCh = D / 8;
+      bool done = false;
+      for (int base = rec0.x; base < v.n_dec && !done; base += 32) {
+        // this lane's token: its units, slot and the slot of its last key
+        const int il = base + lane;
+        int uoff = 0, units = 0, tok = 0, page = -1, off = 0;
+        int64_t slot = -1;
+        if (il < v.n_dec) {
+          uoff = v.tok_unit_off[il];
+          units = v.tok_unit_off[il + 1] - uoff;
+          tok = v.dec_tok[il];
+          slot = a.slot[tok];
+          const int L = min(max(v.kv[tok], 0), v.cap);
+          if (units > 0) {
+            page = a.tpt[(size_t)tok * a.max_pages + (L - 1) / a.P];
+            off = (L - 1) % a.P;
+          }
+        }
+        for (int j = 0; j < 32 && base + j < v.n_dec; ++j) {
+          const int uo = __shfl_sync(0xffffffffu, uoff, j);
+          const int un = __shfl_sync(0xffffffffu, units, j);
+          const int tk = __shfl_sync(0xffffffffu, tok, j);
+          const int pg = __shfl_sync(0xffffffffu, page, j);
+          const int of = __shfl_sync(0xffffffffu, off, j);
+          const int64_t sl = __shfl_sync(0xffffffffu, slot, j);
+          int g = base + j == rec0.x ? rec0.y : 0;
+          if (a.Hkv * uo + g * un >= u1) {
+            done = true;
+            break;
+          }
+          if (un == 0 || sl < 0) continue;
+          const bool ok = pg >= 0 && pg < a.num_pages && sl == (int64_t)pg * a.P + of;
+          for (; g < a.Hkv; ++g) {
+            const int last = a.Hkv * uo + g * un + un - 1;
+            if (last - un + 1 >= u1) break;
+            if (last < u0 || last >= u1) continue;  // another CTA reads this segment's end
+            if (!ok) {
+              if (lane == 0) atomicOr(err, PA_ERR_SLOT_RANGE);
+              __syncwarp();
+              if (lane == 0) st_release_cta(&bars->append_upto, last - u0 + 1);
+              continue;
+            }
+            const size_t dst = (((size_t)pg * a.Hkv + g) * a.P + of) * D;
+            const size_t src = ((size_t)tk * a.Hkv + g) * D;
+            if (lane < kCh)
+              reinterpret_cast<uint4 *>(kpw + dst)[lane] =
+                  reinterpret_cast<const uint4 *>(a.k_new + src)[lane];
+            else if (lane < 2 * kCh)
+              reinterpret_cast<uint4 *>(vpw + dst)[lane - kCh] =
+                  reinterpret_cast<const uint4 *>(a.v_new + src)[lane - kCh];
+            // generic-proxy writes, read next by the producer's TMA (async proxy)
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) st_release_cta(&bars->append_upto, last - u0 + 1);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) st_release_cta(&bars->append_upto, n);  // no more rows
     } else if (w == kDecWarps + 1) {
       // -------------------------------------------------------------- combining warp
       // Jobs from the consumers, in order: (a) a split segment that ended inside the

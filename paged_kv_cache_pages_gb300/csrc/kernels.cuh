@@ -61,6 +61,10 @@ struct AttnArgs {
   const float *k_scale, *v_scale;
   // bounded-wait limit of the split-KV decode kernel, in ns (paged_attn_set_decode_wait_limit)
   unsigned long long wait_ns;
+  // decode with the append fused (f16 pages only), else null: the layer's new K/V rows
+  // [T][Hkv][d] and their slots
+  const uint16_t *k_new, *v_new;
+  const int64_t *slot;
 };
 
 // Decode: split-KV over all SMs plus the log-sum-exp reduce.  Returns a
