@@ -46,6 +46,15 @@ struct WsHeader {
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
 constexpr int KB = 128;  // keys per block (decode unit and prefill key tile)
+// Prefill work units a tile item counts when the planner cuts the work into equal CTA
+// ranges: its key blocks, but at least kPfMinItemUnits.  An item of a few blocks never
+// fills the MMA/softmax pipeline and still pays a whole item switch (epilogue, next Q
+// tiles), so a range of many such items would take far longer than its blocks say.
+// The units past an item's last block are virtual: they hold no work.
+constexpr int kPfMinItemUnits = 6;
+__host__ __device__ inline int pf_item_units(int nkb) {
+  return nkb > 0 ? (nkb > kPfMinItemUnits ? nkb : kPfMinItemUnits) : 0;
+}
 
 struct WsLayout {
   size_t tiles, dec_tok, tok_unit_off, flags, runs, tile_off, dec_start, pf_start, pf_cnt;

@@ -129,10 +129,39 @@ __device__ __forceinline__ void seg_load(Seg &s, const SegCtx &x) {
   const int pair = s.j - s.g * x.NP;
   s.h0 = x.G >= 2 ? s.g * x.G + 2 * pair : s.g;
   s.h1 = s.h0 + 1;
-  s.item_start = (long long)x.tile_off[s.tile] + (long long)s.j * s.nkb;
+  // an item spans pf_item_units(nkb) units: its key blocks, then virtual ones (no work)
+  s.item_start = (long long)x.tile_off[s.tile] + (long long)s.j * pf_item_units(s.nkb);
 }
 
-// Start a run of units [w0, w1) at position start = (tile, item, key block).
+// The next item, in the next tile that has keys when this tile's items are done (there
+// is one: the caller checked that units are left before the end of the run).
+__device__ __forceinline__ void seg_next_item(Seg &s, const SegCtx &x) {
+  if (++s.j == x.items_per_tile) {
+    s.j = 0;
+    do { ++s.tile; } while (x.tiles[s.tile].z == 0);
+  }
+  seg_load(s, x);
+}
+
+// Settle at unit position s.w of the current item: the piece is the item's key blocks
+// from there to the run's end; a position in an item's virtual units moves on to the
+// next item.  False when no key block is left before the run's end.
+__device__ __forceinline__ bool seg_settle(Seg &s, const SegCtx &x) {
+  for (;;) {
+    if (s.w >= s.w_end) return false;
+    const long long kb = s.w - s.item_start;
+    if (kb < s.nkb) {
+      s.kb_b = (int)kb;
+      s.kb_e = (int)min((long long)s.nkb, s.w_end - s.item_start);
+      return true;
+    }
+    s.w = s.item_start + pf_item_units(s.nkb);
+    if (s.w >= s.w_end) return false;
+    seg_next_item(s, x);
+  }
+}
+
+// Start a run of units [w0, w1) in the item start = (tile, item, -) that holds w0.
 __device__ __forceinline__ bool seg_begin(Seg &s, const SegCtx &x, int4 start, long long w0,
                                           long long w1) {
   if (w0 >= w1) return false;
@@ -141,27 +170,23 @@ __device__ __forceinline__ bool seg_begin(Seg &s, const SegCtx &x, int4 start, l
   seg_load(s, x);
   s.w = w0;
   s.w_end = w1;
-  s.kb_b = start.z;
-  s.kb_e = (int)min((long long)s.nkb, s.kb_b + (w1 - w0));
-  return true;
+  return seg_settle(s, x);
 }
 
 __device__ __forceinline__ bool seg_next(Seg &s, const SegCtx &x) {
-  s.w += s.kb_e - s.kb_b;
-  if (s.w >= s.w_end) {
-    if (s.rest.x < 0) return false;
-    const int4 r = s.rest;
-    s.rest.x = -1;
-    return seg_begin(s, x, r, s.rest_w0, s.rest_w1);
+  // past the piece just done: the run ended inside the item, or the next item starts
+  // after the item's virtual units
+  if (s.kb_e == s.nkb) {
+    s.w = s.item_start + pf_item_units(s.nkb);
+    if (s.w < s.w_end) {
+      seg_next_item(s, x);
+      if (seg_settle(s, x)) return true;
+    }
   }
-  if (++s.j == x.items_per_tile) {  // next tile that has keys (there is one: w < w_end <= W)
-    s.j = 0;
-    do { ++s.tile; } while (x.tiles[s.tile].z == 0);
-  }
-  seg_load(s, x);
-  s.kb_b = 0;
-  s.kb_e = (int)min((long long)s.nkb, s.w_end - s.w);
-  return true;
+  if (s.rest.x < 0) return false;
+  const int4 r = s.rest;
+  s.rest.x = -1;
+  return seg_begin(s, x, r, s.rest_w0, s.rest_w1);
 }
 
 // The CTA's share of the prefill work, read from the plan.  Each warp role reads it
@@ -200,7 +225,7 @@ __device__ __forceinline__ PfWork pf_work(const AttnArgs &a, int NP, int G) {
 __device__ __forceinline__ bool seg_first(Seg &s, const SegCtx &x, const PfWork &pw) {
   if (pw.w0 >= pw.w1) return false;
   const int tl = pw.start.w / x.items_per_tile, jl = pw.start.w - tl * x.items_per_tile;
-  const long long ws = (long long)x.tile_off[tl] + (long long)jl * x.tiles[tl].z;
+  const long long ws = (long long)x.tile_off[tl] + (long long)jl * pf_item_units(x.tiles[tl].z);
   if (ws > pw.w0 && ws < pw.w1) {
     s.rest = pw.start;
     s.rest_w0 = pw.w0;

@@ -325,11 +325,12 @@ k_plan(const int32_t *__restrict__ tpt, int max_pages, const int32_t *__restrict
   }
   __syncthreads();
 
-  // 4. prefill work prefix over tiles: each tile holds Hkv * NP items of n_kblocks units
+  // 4. prefill work prefix over tiles: each tile holds Hkv * NP items of
+  //    pf_item_units(n_kblocks) units (key blocks, at least kPfMinItemUnits)
   int work_base = 0;
   for (int c0 = 0; c0 < tile_base; c0 += kPlanThreads) {
     int i = c0 + tid;
-    int wk = i < tile_base ? tiles[i].z * Hkv * NP : 0;
+    int wk = i < tile_base ? pf_item_units(tiles[i].z) * Hkv * NP : 0;
     int tot;
     int off = block_excl_scan(wk, &tot, sh) + work_base;
     if (i < tile_base) tile_off[i] = off;
@@ -391,7 +392,7 @@ k_plan(const int32_t *__restrict__ tpt, int max_pages, const int32_t *__restrict
       while (tiles[t].z == 0 && t + 1 < tile_base) ++t;
       int nkb = tiles[t].z;
       long long r = w - tile_off[t];
-      int j = nkb > 0 ? (int)(r / nkb) : 0;
+      int j = nkb > 0 ? (int)(r / pf_item_units(nkb)) : 0;
       // and the item holding the CTA's last unit, tile * Hkv * NP + item (the prefill
       // kernel runs the segment of that item first, so that both parts of every split
       // item are done early and their combine stays off the end of the launch)
@@ -401,8 +402,8 @@ k_plan(const int32_t *__restrict__ tpt, int max_pages, const int32_t *__restrict
       if (tl >= tile_base) tl = tile_base - 1;
       while (tiles[tl].z == 0 && tl + 1 < tile_base) ++tl;
       const int nkl = tiles[tl].z;
-      const int jl = nkl > 0 ? (int)((wl - tile_off[tl]) / nkl) : 0;
-      pf_start[c] = make_int4(t, j, nkb > 0 ? (int)(r - (long long)j * nkb) : 0,
+      const int jl = nkl > 0 ? (int)((wl - tile_off[tl]) / pf_item_units(nkl)) : 0;
+      pf_start[c] = make_int4(t, j, nkb > 0 ? (int)(r - (long long)j * pf_item_units(nkb)) : 0,
                               tl * Hkv * NP + jl);
     }
   }
