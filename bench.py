@@ -451,7 +451,7 @@ def cpu_baseline_prefill(wl, budget_s=12.0, keep=False):
     kept = []
     while secs < budget_s and i < len(mids):
         u = mids[i]
-        ts, tp, q, _, _ = wl.ubatch(u)
+        q = d["q"].cpu().numpy().view(np.uint16)
         tpt, kv, _ = oracle.expand_ubatch(wl.seq_page_table, ts, tp, wl.P)
         sel = np.arange(0, ts.shape[0], stride, dtype=np.int32)
         t0 = time.perf_counter()
@@ -715,6 +715,80 @@ def bench_fp8_decode(pa, torch, db, steps, warmup, world, hbm, f16_ms_per_layer,
                          "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
                          "frac": round(gbs / hbm, 4), "traffic": traffic_of(traffic_key)},
             "timing": f"CUDA graph of one plan and {db.layers} FP8 decode launches (one per layer)"}
+
+
+def bench_fp8_prefill(pa, torch, pb, steps, warmup, world, peak, f16_ms_per_step,
+                      f16_ms_per_launch, with_cpu):
+    """The 8x16K prefill step over FP8 pages: the same ubatches, each one expansion,
+    quantising append (E4M3 codes, one scale per row), plan, tensor-core prefill (the
+    codes widened to binary16 in shared memory) and decode launch, over a pool of
+    codes (half the K/V bytes of the binary16 pool)."""
+    wl, dev = pb.wl, pb.dev
+    pool = pa.new_fp8_pool(wl.num_pages, wl.Hkv, wl.P, wl.d, dev)
+    ws = pa.new_workspace(max(d["T"] for d in pb.ub), wl.Hq, wl.Hkv, wl.d, dev)
+    outs = [torch.empty_like(d["out"]) for d in pb.ub]
+
+    def ubatch(d, out, ev=None):
+        pa.expand_ubatch(pb.spt, d["tok_seq"], d["tok_pos"], wl.P,
+                         out=(d["tpt"], d["kv"], d["slot"]))
+        pa.kv_append_fp8(d["k"], d["v"], d["slot"], *pool)
+        pa.plan(d["tpt"], d["kv"], wl.Hq, wl.Hkv, wl.P, wl.d, ws)
+        if ev is not None:
+            ev[0].record()
+        pa.prefill_fp8(d["q"], *pool, d["tpt"], d["kv"], wl.scale, out, ws)
+        if ev is not None:
+            ev[1].record()
+        pa.decode_fp8(d["q"], *pool, d["tpt"], d["kv"], wl.scale, out, ws)
+
+    def step(events=None):
+        for i, (d, out) in enumerate(zip(pb.ub, outs)):
+            ubatch(d, out, None if events is None else events[i])
+
+    n_ub = len(pb.ub)
+    g = capture_step(torch, step)
+    total, _ = time_steps(torch, g.replay, steps, warmup, world)
+    kern, how = time_launches(torch, step, n_ub, steps, warmup, world)
+    if pa.read_error(ws):
+        raise RuntimeError("device error word set in the FP8 prefill")
+    t_step = max_over_ranks(total / 1e3 / steps, world)
+    t_kern = kern / 1e3 / (steps * n_ub)
+    ach = pb.flops / n_ub / t_kern / 1e12
+    res = {"workload": "prefill_8x16k_fp8_pages", "unit": "TFLOP/s",
+           "value": round(aggregate(pb.flops, t_step, world) / 1e12, 3),
+           "ms_per_step": round(t_step * 1e3, 3),
+           "f16_ms_per_step": round(f16_ms_per_step, 3),
+           "f16_ms_per_prefill_launch": round(f16_ms_per_launch, 4),
+           "ms_per_prefill_launch": round(t_kern * 1e3, 4),
+           "gpu_launches": 5 * n_ub * steps,
+           "roofline": {"bound": "tensor", "kernel": "k_prefill (FP8 pages)",
+                        "achieved": round(ach, 2), "peak": peak, "unit": "TFLOP/s",
+                        "frac": round(ach / peak, 4), "timing": how,
+                        "traffic": traffic_of("k_prefill_fp8")},
+           "timing": "value: CUDA graph of the 65 ubatches x (expand, append_fp8, plan, "
+                     "prefill_fp8, decode_fp8)"}
+    if with_cpu:
+        import oracle
+        u = n_ub - 1
+        d = pb.ub[u]
+        ts, tp, q, _, _ = wl.ubatch(u)
+        rng = np.random.default_rng(11)
+        sel = np.sort(rng.choice(d["T"], min(24, d["T"]), replace=False)).astype(np.int32)
+        host = [x.cpu().numpy() for x in pool]
+        tpt_h, kv_h = d["tpt"].cpu().numpy(), d["kv"].cpu().numpy()
+        t0 = time.perf_counter()
+        ref = oracle.paged_attention_fp8(q, *host, tpt_h, kv_h, wl.scale, tokens=sel)
+        secs = time.perf_counter() - t0
+        f_s = 4.0 * wl.d * wl.Hq * float(kv_h[sel].astype(np.int64).sum())
+        res["cpu_baseline"] = {"value": f_s / secs / 1e12, "unit": "TFLOP/s",
+                               "cores": oracle.num_threads(), "kind": "oracle",
+                               "sample": f"{len(sel)} tokens of the last ubatch, all heads, "
+                                         f"fp64 over the FP8 pool, {secs:.1f} s"}
+        res["parity"] = parity_check(
+            [(u, sel, ref)],
+            lambda u_, s_: outs[u_][torch.from_numpy(s_).long().to(dev)].float().cpu().numpy())
+        if not res["parity"]["ok"]:
+            raise RuntimeError(f"FP8 prefill outputs differ from the oracle: {res['parity']}")
+    return res
 
 
 LONGTAIL_LAYERS = 4
@@ -984,6 +1058,9 @@ def run_ours(args):
                                                            args.warmup, world, t_step * 1e3),
         "fp8_pages": bench_fp8_decode(pa, torch, db, args.steps, args.warmup, world, hbm,
                                       d_kt * 1e3),
+        "fp8_pages_prefill": bench_fp8_prefill(
+            pa, torch, pb, args.steps, args.warmup, world, peak, t_step * 1e3, t_kern * 1e3,
+            with_cpu=rank == 0 and world == 1 and not args.no_cpu_baseline),
     }
     line["longtail"] = bench_longtail(pa, torch, dev, args.steps, args.warmup, world, hbm,
                                       with_cpu=rank == 0 and world == 1 and not args.no_cpu_baseline,

@@ -334,16 +334,47 @@ int paged_kv_append_fp8(const uint16_t *k, const uint16_t *v, const int64_t *slo
 /*
  * Split-KV decode attention over FP8 pages (layout above; page size 128, d 128,
  * scale arrays 16-byte aligned): K_t[j] = E4M3(k8) * k_scale, V_t[j] likewise.
- * Runs on the workspace's plan, which must come from paged_attn_plan_decode for
- * the same tables (one plan serves every layer); writes out for every token;
- * other arguments as paged_attn_forward.  PA_EUNSUPPORTED for another page size
- * or head dimension.
+ * Runs on the workspace's plan for the same tables (one plan serves every layer):
+ * from paged_attn_plan_decode it writes out for every token; from paged_attn_plan,
+ * for the tokens the plan leaves to the decode kernel (as paged_attn_decode).  Other
+ * arguments as paged_attn_forward.  PA_EUNSUPPORTED for another page size or head
+ * dimension.
  */
 int paged_attn_decode_fp8(const uint16_t *q, const uint8_t *k8_pages, const uint8_t *v8t_pages,
                           const float *k_scale, const float *v_scale,
                           const int32_t *tok_page_table, int max_pages, const int32_t *tok_kv_len,
                           int T, int Hq, int Hkv, int P, int d, int num_pages, float scale,
                           uint16_t *out, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Tensor-core prefill tiles over FP8 pages: the tokens of the workspace's plan's
+ * tiles (from paged_attn_plan or paged_attn_plan_prefill for the same tables), as
+ * paged_attn_prefill.  Layout, page size, head dimension and scale arrays as
+ * paged_attn_decode_fp8.  Each key block's codes are widened in shared memory to
+ * binary16(code * scale) -- the value a binary16 cache of the dequantised rows would
+ * hold -- and the tile then runs the binary16 MMAs of paged_attn_prefill; V rows past
+ * a tile's longest kv_len are cleared, so unwritten cells (NaN codes included) never
+ * reach the output.  A scale below the binary16 range (2^-24) widens to zero.
+ * PA_ERR_PAGE_RANGE as paged_attn_forward.  One launch.
+ */
+int paged_attn_prefill_fp8(const uint16_t *q, const uint8_t *k8_pages, const uint8_t *v8t_pages,
+                           const float *k_scale, const float *v_scale,
+                           const int32_t *tok_page_table, int max_pages,
+                           const int32_t *tok_kv_len, int T, int Hq, int Hkv, int P, int d,
+                           int num_pages, float scale, uint16_t *out, void *workspace,
+                           size_t workspace_bytes, void *stream);
+
+/*
+ * paged_attn_forward over FP8 pages: paged_attn_plan, then paged_attn_prefill_fp8
+ * and paged_attn_decode_fp8 on that plan.  A whole mixed ubatch (prefill runs and
+ * decode tokens) in three launches plus the plan's two.
+ */
+int paged_attn_forward_fp8(const uint16_t *q, const uint8_t *k8_pages, const uint8_t *v8t_pages,
+                           const float *k_scale, const float *v_scale,
+                           const int32_t *tok_page_table, int max_pages,
+                           const int32_t *tok_kv_len, int T, int Hq, int Hkv, int P, int d,
+                           int num_pages, float scale, uint16_t *out, void *workspace,
+                           size_t workspace_bytes, void *stream);
 
 /*
  * Page copy for copy-on-write forks (CacheFlow page, section 核心架构 2: blocks

@@ -13,7 +13,8 @@ Entry points mirror include/paged_attn.h:
   copy_pages      page copy of a copy-on-write fork
   masked_decode / masked_prefill   the unified-span baseline (masked attention over a
                   shared span) on the split-KV and on the tcgen05 path
-  kv_append_fp8 / decode_fp8   FP8 (E4M3) KV pages with per-row scales
+  kv_append_fp8 / decode_fp8 / prefill_fp8 / forward_fp8   FP8 (E4M3) KV pages with
+                  per-row scales
   plan / prefill / decode / run / forward   the attention itself
   validate, read_error, set_prefill_min_run, workspace_size
   PagePool        host page allocator with reference-counted sharing
@@ -70,6 +71,10 @@ _SIGS = {
                             _i),
     "paged_attn_decode_fp8": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i,
                                ctypes.c_float, _vp, _vp, _sz, _vp], _i),
+    "paged_attn_prefill_fp8": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i,
+                                ctypes.c_float, _vp, _vp, _sz, _vp], _i),
+    "paged_attn_forward_fp8": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i,
+                                ctypes.c_float, _vp, _vp, _sz, _vp], _i),
     "paged_attn_plan_decode": ([_vp, _i, _vp, _i, _i, _i, _i, _i, _vp, _sz, _vp], _i),
     "paged_attn_masked_decode": ([_vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i,
                                   ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i),
@@ -245,20 +250,44 @@ def kv_append_fp8(k, v, slot_mapping, k8, v8t, k_scale, v_scale, err=None, strea
                                     d, _ptr(err), _stream(stream)), "paged_kv_append_fp8")
 
 
-def decode_fp8(q, k8, v8t, k_scale, v_scale, tok_page_table, tok_kv_len, scale, out, workspace,
-               stream=None):
-    """Split-KV decode attention over FP8 pages (runs on a plan from plan_decode)."""
+def _attn_fp8(name, q, k8, v8t, k_scale, v_scale, tok_page_table, tok_kv_len, scale, out,
+              workspace, stream):
     _req(q, torch.float16, "q")
-    _req(out, torch.float16, "out")
     _req(tok_page_table, torch.int32, "tok_page_table")
     _req(tok_kv_len, torch.int32, "tok_kv_len")
     T, Hq, d = q.shape
     N, Hkv, P, _ = k8.shape
-    _check(_lib.paged_attn_decode_fp8(
+    if out is None:
+        out = torch.empty_like(q)
+    _req(out, torch.float16, "out")
+    if workspace is None:
+        workspace = new_workspace(T, Hq, Hkv, d, q.device)
+    _check(getattr(_lib, name)(
         _ptr(q), _ptr(k8), _ptr(v8t), _ptr(k_scale), _ptr(v_scale), _ptr(tok_page_table),
         tok_page_table.shape[1], _ptr(tok_kv_len), T, Hq, Hkv, P, d, N, float(scale), _ptr(out),
-        _ptr(workspace), workspace.numel(), _stream(stream)), "paged_attn_decode_fp8")
+        _ptr(workspace), workspace.numel(), _stream(stream)), name)
     return out
+
+
+def decode_fp8(q, k8, v8t, k_scale, v_scale, tok_page_table, tok_kv_len, scale, out, workspace,
+               stream=None):
+    """Split-KV decode attention over FP8 pages (on a plan from plan_decode or plan)."""
+    return _attn_fp8("paged_attn_decode_fp8", q, k8, v8t, k_scale, v_scale, tok_page_table,
+                     tok_kv_len, scale, out, workspace, stream)
+
+
+def prefill_fp8(q, k8, v8t, k_scale, v_scale, tok_page_table, tok_kv_len, scale, out, workspace,
+                stream=None):
+    """Tensor-core prefill tiles over FP8 pages (on a plan from plan or plan_prefill)."""
+    return _attn_fp8("paged_attn_prefill_fp8", q, k8, v8t, k_scale, v_scale, tok_page_table,
+                     tok_kv_len, scale, out, workspace, stream)
+
+
+def forward_fp8(q, k8, v8t, k_scale, v_scale, tok_page_table, tok_kv_len, scale, out=None,
+                workspace=None, stream=None):
+    """Plan + prefill + decode for one ubatch over FP8 pages; returns out [T][Hq][d]."""
+    return _attn_fp8("paged_attn_forward_fp8", q, k8, v8t, k_scale, v_scale, tok_page_table,
+                     tok_kv_len, scale, out, workspace, stream)
 
 
 def copy_pages(src, dst, k_pages, v_pages, err=None, stream=None):

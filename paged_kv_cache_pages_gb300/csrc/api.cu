@@ -187,12 +187,13 @@ int paged_kv_append_fp8(const uint16_t *k, const uint16_t *v, const int64_t *slo
   return launch_status(cudaGetLastError());
 }
 
-int paged_attn_decode_fp8(const uint16_t *q, const uint8_t *k8_pages, const uint8_t *v8t_pages,
-                          const float *k_scale, const float *v_scale,
-                          const int32_t *tok_page_table, int max_pages, const int32_t *tok_kv_len,
-                          int T, int Hq, int Hkv, int P, int d, int num_pages, float scale,
-                          uint16_t *out, void *workspace, size_t workspace_bytes, void *stream) {
-  NvtxRange nvtx_range("paged_attn_decode_fp8");
+// Checks and launch arguments shared by the FP8-page attention entry points.  Returns
+// PA_OK with *a and *maps set, or the status to return (PA_OK with T == 0: nothing to do).
+static int fp8_setup(const uint16_t *q, const uint8_t *k8_pages, const uint8_t *v8t_pages,
+                     const float *k_scale, const float *v_scale, const int32_t *tok_page_table,
+                     int max_pages, const int32_t *tok_kv_len, int T, int Hq, int Hkv, int P,
+                     int d, int num_pages, float scale, uint16_t *out, void *workspace,
+                     size_t workspace_bytes, AttnArgs *a, AttnMaps *maps) {
   const uint16_t *kp = reinterpret_cast<const uint16_t *>(k8_pages);
   const uint16_t *vp = reinterpret_cast<const uint16_t *>(v8t_pages);
   int st = check_attn(q, kp, vp, tok_page_table, max_pages, tok_kv_len, T, Hq, Hkv, P, d,
@@ -201,14 +202,64 @@ int paged_attn_decode_fp8(const uint16_t *q, const uint8_t *k8_pages, const uint
   if (P != 128 || d != 128) return PA_EUNSUPPORTED;
   if (!k_scale || !v_scale) return PA_EINVAL;
   if (!aligned16(k_scale) || !aligned16(v_scale)) return PA_EALIGN;
-  AttnArgs a = make_args(q, kp, vp, tok_page_table, max_pages, tok_kv_len, T, Hq, Hkv, P, d,
-                         num_pages, scale, out, workspace);
-  a.k_scale = k_scale;
-  a.v_scale = v_scale;
+  *a = make_args(q, kp, vp, tok_page_table, max_pages, tok_kv_len, T, Hq, Hkv, P, d, num_pages,
+                 scale, out, workspace);
+  a->k_scale = k_scale;
+  a->v_scale = v_scale;
+  return encode_attn_maps_fp8(*a, maps);
+}
+
+int paged_attn_decode_fp8(const uint16_t *q, const uint8_t *k8_pages, const uint8_t *v8t_pages,
+                          const float *k_scale, const float *v_scale,
+                          const int32_t *tok_page_table, int max_pages, const int32_t *tok_kv_len,
+                          int T, int Hq, int Hkv, int P, int d, int num_pages, float scale,
+                          uint16_t *out, void *workspace, size_t workspace_bytes, void *stream) {
+  NvtxRange nvtx_range("paged_attn_decode_fp8");
+  AttnArgs a;
   AttnMaps maps;
-  st = encode_attn_maps_fp8(a, &maps);
-  if (st != PA_OK) return st;
+  int st = fp8_setup(q, k8_pages, v8t_pages, k_scale, v_scale, tok_page_table, max_pages,
+                     tok_kv_len, T, Hq, Hkv, P, d, num_pages, scale, out, workspace,
+                     workspace_bytes, &a, &maps);
+  if (st != PA_OK || T == 0) return st;
   return launch_status(launch_decode(a, sm_count(), &maps, static_cast<cudaStream_t>(stream)));
+}
+
+int paged_attn_prefill_fp8(const uint16_t *q, const uint8_t *k8_pages, const uint8_t *v8t_pages,
+                           const float *k_scale, const float *v_scale,
+                           const int32_t *tok_page_table, int max_pages,
+                           const int32_t *tok_kv_len, int T, int Hq, int Hkv, int P, int d,
+                           int num_pages, float scale, uint16_t *out, void *workspace,
+                           size_t workspace_bytes, void *stream) {
+  NvtxRange nvtx_range("paged_attn_prefill_fp8");
+  AttnArgs a;
+  AttnMaps maps;
+  int st = fp8_setup(q, k8_pages, v8t_pages, k_scale, v_scale, tok_page_table, max_pages,
+                     tok_kv_len, T, Hq, Hkv, P, d, num_pages, scale, out, workspace,
+                     workspace_bytes, &a, &maps);
+  if (st != PA_OK || T == 0) return st;
+  return launch_status(launch_prefill(a, sm_count(), &maps, static_cast<cudaStream_t>(stream)));
+}
+
+int paged_attn_forward_fp8(const uint16_t *q, const uint8_t *k8_pages, const uint8_t *v8t_pages,
+                           const float *k_scale, const float *v_scale,
+                           const int32_t *tok_page_table, int max_pages,
+                           const int32_t *tok_kv_len, int T, int Hq, int Hkv, int P, int d,
+                           int num_pages, float scale, uint16_t *out, void *workspace,
+                           size_t workspace_bytes, void *stream) {
+  NvtxRange nvtx_range("paged_attn_forward_fp8");
+  AttnArgs a;
+  AttnMaps maps;
+  int st = fp8_setup(q, k8_pages, v8t_pages, k_scale, v_scale, tok_page_table, max_pages,
+                     tok_kv_len, T, Hq, Hkv, P, d, num_pages, scale, out, workspace,
+                     workspace_bytes, &a, &maps);
+  if (st != PA_OK || T == 0) return st;
+  st = paged_attn_plan(tok_page_table, max_pages, tok_kv_len, T, Hq, Hkv, P, d, workspace,
+                       workspace_bytes, stream);
+  if (st != PA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = launch_status(launch_prefill(a, sm_count(), &maps, s));
+  if (st != PA_OK) return st;
+  return launch_status(launch_decode(a, sm_count(), &maps, s));
 }
 
 int paged_copy_pages(const int32_t *src, const int32_t *dst, int n, uint16_t *k_pages,

@@ -77,6 +77,7 @@ struct PfBars {
   uint64_t k_full[kPfStages], k_empty[kPfStages], v_full[kPfStages], v_empty[kPfStages];
   uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
   uint64_t turn[2];  // issuer turns: tile 1's issuer -> tile 0's, tile 0's -> tile 1's
+  uint64_t kc_full, vc_full;  // FP8 pages: a block's codes have landed (K, V)
   uint32_t tmem_base;
   int abort;
 };
@@ -94,6 +95,93 @@ __device__ __forceinline__ bool pf_wait(uint64_t *bar, uint32_t parity, int *err
       *abort = 1;
       return false;
     }
+  }
+}
+
+// ---- FP8 pages: E4M3 codes widened to binary16 in shared memory -----------------
+// A block's codes (128 rows x 128 bytes, the 128-byte swizzle) land in the upper half
+// of the stage's binary16 tile and are widened in place: row r of the codes sits where
+// row r of the tile's second 64-column box goes, so each row is read whole before any
+// of it is written.  Lane = (row r = 4i + lane / 8, 16-code chunk c = lane % 8): a
+// quarter-warp covers one row, and its loads and stores hit eight distinct 16-byte
+// bank groups.  Each element becomes binary16(code * scale): the exact E4M3 value
+// (cvt), times the scale split in two binary16 parts (hi = rn(s), lo = rn(s - hi)),
+// x * hi + x * lo, so the result is the binary16 rounding of code * scale up to the
+// rounding of the small x * lo term.
+
+// the scale s as hi = rn(s) and lo = rn(s - hi), both binary16
+__device__ __forceinline__ void scale_split(float s, __half &hi, __half &lo) {
+  hi = __float2half_rn(s);
+  lo = __float2half_rn(s - __half2float(hi));
+}
+
+__device__ __forceinline__ uint32_t h2_bits(__half a, __half b) {
+  const __half2 h = __halves2half2(a, b);
+  return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// (hi, hi) and (lo, lo) of one scale, packed
+__device__ __forceinline__ uint2 scale_h2(float s) {
+  __half hi, lo;
+  scale_split(s, hi, lo);
+  return make_uint2(h2_bits(hi, hi), h2_bits(lo, lo));
+}
+
+// four E4M3 codes (byte i = element i) -> two binary16 pairs, exact
+__device__ __forceinline__ void e4m3x4_widen(uint32_t w, uint32_t &p01, uint32_t &p23) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, lo;\n\tcvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+      : "=r"(p01), "=r"(p23) : "r"(w));
+}
+
+// x * hi + x * lo on binary16 pairs
+__device__ __forceinline__ uint32_t h2_scale(uint32_t x, uint32_t hi, uint32_t lo) {
+  uint32_t t, r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(t) : "r"(x), "r"(lo));
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(x), "r"(hi), "r"(t));
+  return r;
+}
+
+// Widen the 128 x 128 codes at tile + kBoxBytes into the binary16 tile (two boxes of
+// 128 rows x 64 columns).  ROW: one scale per row (K: rows are keys), scales by row
+// from rtab[r] = (hi2, lo2); else one per column (V transposed: columns are keys), the
+// lane's 16 columns' pairs in chi/clo and codes of columns past the valid keys cleared
+// by cmask (an E4M3 NaN code times a zero scale would still be NaN).
+template <bool ROW>
+__device__ __forceinline__ void widen_tile(unsigned char *tile, const uint2 *rtab,
+                                           const uint32_t (&chi)[8], const uint32_t (&clo)[8],
+                                           const uint32_t (&cmask)[4], int lane) {
+  const int c = lane & 7, rs = lane >> 3;
+  const unsigned char *codes = tile + kBoxBytes;
+  unsigned char *box = tile + (c >> 2) * kBoxBytes;
+  // output chunks 2(c % 4) and 2(c % 4) + 1 of the row; lanes c < 4 store the even one
+  // first and lanes c >= 4 the odd one, so that a quarter-warp's stores never collide
+  const int first = 2 * (c & 3) + (c >> 2), second = first ^ 1;
+#pragma unroll 1
+  for (int i = 0; i < 32; ++i) {
+    const int r = 4 * i + rs, sw = r & 7;
+    uint4 x = *reinterpret_cast<const uint4 *>(codes + r * 128 + ((c ^ sw) << 4));
+    uint32_t hi[4], lo[4];
+    if (ROW) {
+      const uint2 t = rtab[r];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) { hi[e] = t.x; lo[e] = t.y; }
+    }
+    __syncwarp();  // the whole row is read before the second box's row overwrites it
+    const uint32_t wd[4] = {x.x & cmask[0], x.y & cmask[1], x.z & cmask[2], x.w & cmask[3]};
+    uint32_t h[8];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      uint32_t p01, p23;
+      e4m3x4_widen(wd[e], p01, p23);
+      h[2 * e] = ROW ? h2_scale(p01, hi[0], lo[0]) : h2_scale(p01, chi[2 * e], clo[2 * e]);
+      h[2 * e + 1] =
+          ROW ? h2_scale(p23, hi[0], lo[0]) : h2_scale(p23, chi[2 * e + 1], clo[2 * e + 1]);
+    }
+    const uint4 o0 = make_uint4(h[0], h[1], h[2], h[3]), o1 = make_uint4(h[4], h[5], h[6], h[7]);
+    unsigned char *rowp = box + r * 128;
+    *reinterpret_cast<uint4 *>(rowp + ((first ^ sw) << 4)) = (c >> 2) ? o1 : o0;
+    *reinterpret_cast<uint4 *>(rowp + ((second ^ sw) << 4)) = (c >> 2) ? o0 : o1;
   }
 }
 
@@ -240,9 +328,17 @@ __device__ __forceinline__ bool seg_first(Seg &s, const SegCtx &x, const PfWork 
 // cells; key j is kept only if its cell belongs to the token's sequence at a position
 // up to the token's own (cell_seq[slot] == tok_seq[t] && cell_pos[slot] <= tok_pos[t]),
 // and the V rows of free cells (cell_seq < 0, which may hold NaN) are zeroed.
-template <int D, bool MASK>
+//
+// KV8: FP8 pages (page size 128 = one key block, d = 128).  Warp 8 loads Q and the K
+// codes and widens them; warp 11 loads and widens the V codes, stored transposed
+// ([d][key]), so the binary16 V tile is K-major for the PV product.  Both widen into
+// the stage's binary16 tile (see widen_tile); the MMA issuers and the softmax then run
+// exactly as for binary16 pages.
+template <int D, bool MASK, bool KV8>
 __global__ void __launch_bounds__(kPfThreads, 1)
 k_prefill(AttnArgs a, const __grid_constant__ AttnMaps maps) {
+  static_assert(!(MASK && KV8), "one variant at a time");
+  static_assert(!KV8 || D == 128, "FP8 pages: d 128");
   using Cfg = PfCfg<D>;
   // rows of a split part's record: O[D] | m | l | 2 unused (D + 4 rows of 128 floats)
   constexpr int kPartStride = D + 4;
@@ -284,6 +380,8 @@ k_prefill(AttnArgs a, const __grid_constant__ AttnMaps maps) {
     }
     mbar_init(&bars->turn[0], 1);
     mbar_init(&bars->turn[1], 1);
+    mbar_init(&bars->kc_full, 1);
+    mbar_init(&bars->vc_full, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->p_full[i], 128);
@@ -311,7 +409,156 @@ k_prefill(AttnArgs a, const __grid_constant__ AttnMaps maps) {
 
   if (warp >= 8) {
    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
-   if (warp == kWarpTma && lane == 0) {
+   if (KV8 && warp == kWarpTma) {
+    // ------------------------------------------------------------ FP8: Q, K codes (warp)
+    const PfWork pw = pf_work(a, NP, G);
+    const SegCtx &sx = pw.sx;
+    uint32_t it = 0;
+    int nitem = 0;
+    const int oob_row = a.num_pages * a.Hkv * KB;  // first row past the pool: zero fill
+    uint2 *ktab = reinterpret_cast<uint2 *>(smem + Cfg::kCinfo);
+    const uint32_t ones[4] = {~0u, ~0u, ~0u, ~0u};
+    const uint32_t none[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    Seg w{};
+    const int32_t *row = nullptr;
+    // K codes of key block kb (one page) into the upper half of stage it % kPfStages,
+    // widened there; the MMA issuers see k_full only once the binary16 tile is complete
+    auto k_block = [&](int kb) -> bool {
+      const int st = it % kPfStages;
+      const uint32_t ph = (it / kPfStages) & 1u;
+      if (!__all_sync(~0u, pf_wait(&bars->k_empty[st], ph ^ 1u, err, abort))) return false;
+      const int page = row[kb];
+      const bool pv = page >= 0 && page < a.num_pages;
+      const int r0 = pv ? (page * a.Hkv + w.g) * KB : oob_row;
+      unsigned char *tile = smem + Cfg::kK + st * Cfg::kTile;
+      if (lane == 0) {
+        if (!pv) atomicOr(err, PA_ERR_PAGE_RANGE);
+        mbar_arrive_expect_tx(&bars->kc_full, kBoxBytes);
+        tc::tma_load_2d(tile + kBoxBytes, &maps.k, 0, r0, &bars->kc_full);
+        if (kb + 1 < w.kb_e) {
+          const int pn = row[kb + 1];
+          if (pn >= 0 && pn < a.num_pages) tc::tma_prefetch_2d(&maps.k, 0, (pn * a.Hkv + w.g) * KB);
+        }
+      }
+      // row scales (a missing page: zero rows, zero scales) -> (hi, lo) table
+      const float4 s4 = pv ? __ldg(reinterpret_cast<const float4 *>(a.k_scale + r0) + lane)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+      const uint2 t0 = scale_h2(s4.x), t1 = scale_h2(s4.y), t2 = scale_h2(s4.z),
+                  t3 = scale_h2(s4.w);
+      __syncwarp();  // the previous block's table reads are done
+      reinterpret_cast<uint4 *>(ktab)[2 * lane] = make_uint4(t0.x, t0.y, t1.x, t1.y);
+      reinterpret_cast<uint4 *>(ktab)[2 * lane + 1] = make_uint4(t2.x, t2.y, t3.x, t3.y);
+      if (!__all_sync(~0u, pf_wait(&bars->kc_full, it & 1u, err, abort))) return false;
+      __syncwarp();
+      widen_tile<true>(tile, ktab, none, none, ones, lane);
+      fence_proxy_async();  // generic-proxy writes -> the tensor core's reads
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->k_full[st]);
+      ++it;
+      return true;
+    };
+    for (bool more = seg_first(w, sx, pw); more; more = seg_next(w, sx)) {
+      row = a.tpt + (size_t)w.tile_start * a.max_pages;
+      int kb = w.kb_b;
+      if (nitem > 0) {
+        if (!k_block(kb++)) break;
+        if (!__all_sync(~0u, lane != 0 || pf_wait(&bars->q_empty, (nitem - 1) & 1, err, abort)))
+          break;
+      }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars->q_full, NQ * Cfg::kTile);
+        for (int hf = 0; hf < Cfg::kHalves; ++hf) {
+          tc::tma_load_3d(smem + Cfg::kQ0 + hf * kBoxBytes, &maps.q, hf * 64, w.h0, w.tile_start,
+                          &bars->q_full);
+          if (NQ == 2)
+            tc::tma_load_3d(smem + Cfg::kQ1 + hf * kBoxBytes, &maps.q, hf * 64, w.h1,
+                            w.tile_start, &bars->q_full);
+        }
+      }
+      bool ok = true;
+      for (; kb < w.kb_e && ok; ++kb) ok = k_block(kb);
+      if (!ok) break;
+      ++nitem;
+    }
+   } else if (KV8 && warp == kWarpTma + 3) {
+    // ------------------------------------------------------------ FP8: V codes (warp)
+    const PfWork pw = pf_work(a, NP, G);
+    const SegCtx &sx = pw.sx;
+    uint32_t it = 0;
+    const int oob_row = a.num_pages * a.Hkv * D;
+    uint32_t *vhi = reinterpret_cast<uint32_t *>(smem + Cfg::kCinfo + 1024);
+    uint32_t *vlo = vhi + KB / 2;
+    const int c8 = lane & 7;
+    Seg w{};
+    bool ok = true;
+    for (bool more = seg_first(w, sx, pw); more && ok; more = seg_next(w, sx)) {
+      const int32_t *row = a.tpt + (size_t)w.tile_start * a.max_pages;
+      for (int kb = w.kb_b; kb < w.kb_e; ++kb) {
+        const int st = it % kPfStages;
+        const uint32_t ph = (it / kPfStages) & 1u;
+        if (!__all_sync(~0u, pf_wait(&bars->v_empty[st], ph ^ 1u, err, abort))) {
+          ok = false;
+          break;
+        }
+        const int page = row[kb];
+        const bool pv = page >= 0 && page < a.num_pages;
+        const int hp = page * a.Hkv + w.g;
+        unsigned char *tile = smem + Cfg::kV + st * Cfg::kTile;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bars->vc_full, kBoxBytes);
+          tc::tma_load_2d(tile + kBoxBytes, &maps.v, 0, pv ? hp * D : oob_row, &bars->vc_full);
+          if (kb + 1 < w.kb_e) {
+            const int pn = row[kb + 1];
+            if (pn >= 0 && pn < a.num_pages) tc::tma_prefetch_2d(&maps.v, 0, (pn * a.Hkv + w.g) * D);
+          }
+        }
+        // keys past the tile's longest kv_len: zero scale and cleared codes (they may
+        // hold anything, NaN codes included, and P is 0 there but 0 * NaN is NaN)
+        const int nvalid = min(KB, w.max_kv - kb * KB);
+        float4 s4 = pv ? __ldg(reinterpret_cast<const float4 *>(a.v_scale + (size_t)hp * KB) + lane)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (4 * lane + 0 >= nvalid) s4.x = 0.f;
+        if (4 * lane + 1 >= nvalid) s4.y = 0.f;
+        if (4 * lane + 2 >= nvalid) s4.z = 0.f;
+        if (4 * lane + 3 >= nvalid) s4.w = 0.f;
+        __half h0, l0, h1, l1, h2, l2, h3, l3;
+        scale_split(s4.x, h0, l0);
+        scale_split(s4.y, h1, l1);
+        scale_split(s4.z, h2, l2);
+        scale_split(s4.w, h3, l3);
+        __syncwarp();  // the previous block's table reads are done
+        reinterpret_cast<uint2 *>(vhi)[lane] = make_uint2(h2_bits(h0, h1), h2_bits(h2, h3));
+        reinterpret_cast<uint2 *>(vlo)[lane] = make_uint2(h2_bits(l0, l1), h2_bits(l2, l3));
+        __syncwarp();
+        uint32_t chi[8], clo[8], cmask[4];
+        {
+          const uint4 a0 = reinterpret_cast<const uint4 *>(vhi)[2 * c8],
+                      a1 = reinterpret_cast<const uint4 *>(vhi)[2 * c8 + 1],
+                      b0 = reinterpret_cast<const uint4 *>(vlo)[2 * c8],
+                      b1 = reinterpret_cast<const uint4 *>(vlo)[2 * c8 + 1];
+          chi[0] = a0.x; chi[1] = a0.y; chi[2] = a0.z; chi[3] = a0.w;
+          chi[4] = a1.x; chi[5] = a1.y; chi[6] = a1.z; chi[7] = a1.w;
+          clo[0] = b0.x; clo[1] = b0.y; clo[2] = b0.z; clo[3] = b0.w;
+          clo[4] = b1.x; clo[5] = b1.y; clo[6] = b1.z; clo[7] = b1.w;
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int nb = min(max(nvalid - (16 * c8 + 4 * q), 0), 4);  // valid codes of the word
+          cmask[q] = nb >= 4 ? ~0u : (1u << (8 * nb)) - 1u;
+        }
+        if (!__all_sync(~0u, pf_wait(&bars->vc_full, it & 1u, err, abort))) {
+          ok = false;
+          break;
+        }
+        __syncwarp();
+        widen_tile<false>(tile, nullptr, chi, clo, cmask, lane);
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->v_full[st]);
+        ++it;
+      }
+    }
+   } else if (!KV8 && warp == kWarpTma && lane == 0) {
     // ------------------------------------------------------------ TMA producer
     {
       const PfWork pw = pf_work(a, NP, G);
@@ -394,7 +641,9 @@ k_prefill(AttnArgs a, const __grid_constant__ AttnMaps maps) {
     const PfWork pw = pf_work(a, NP, G);
     const SegCtx &sx = pw.sx;
     constexpr uint32_t idS = tc::idesc_f16(128, 128, false);
-    constexpr uint32_t idPV = tc::idesc_f16(128, D, true);
+    // V: MN-major ([key][d] rows) for binary16 pages; K-major ([d][key] rows) for FP8
+    // pages, whose V codes are stored transposed
+    constexpr uint32_t idPV = tc::idesc_f16(128, D, !KV8);
     const uint32_t sQ0 = smem_u32(smem + Cfg::kQ0), sQ1 = smem_u32(smem + Cfg::kQ1);
     const uint32_t sK = smem_u32(smem + Cfg::kK), sV = smem_u32(smem + Cfg::kV);
     // Operand descriptors by their low words (the high word is one constant): a k-step
@@ -405,7 +654,8 @@ k_prefill(AttnArgs a, const __grid_constant__ AttnMaps maps) {
     static_assert(kPfStages == 2, "two K/V stages");
     const uint32_t lQ0 = tc::sdesc_lo(sQ0, 16), lQ1 = tc::sdesc_lo(sQ1, 16);
     const uint32_t lK0 = tc::sdesc_lo(sK, 16), lK1 = tc::sdesc_lo(sK + Cfg::kTile, 16);
-    const uint32_t lV0 = tc::sdesc_lo(sV, kBoxBytes), lV1 = tc::sdesc_lo(sV + Cfg::kTile, kBoxBytes);
+    const uint32_t lV0 = tc::sdesc_lo(sV, KV8 ? 16 : kBoxBytes),
+                   lV1 = tc::sdesc_lo(sV + Cfg::kTile, KV8 ? 16 : kBoxBytes);
     auto issue_S = [&](int i, int st) {
       const uint32_t d = tmem + i * 128;
       const uint32_t a0 = tc::opaque(i ? lQ1 : lQ0), b0 = tc::opaque(st ? lK1 : lK0);
@@ -423,8 +673,12 @@ k_prefill(AttnArgs a, const __grid_constant__ AttnMaps maps) {
       const uint32_t b0 = tc::opaque(st ? lV1 : lV0);
       tc::mma_ts_lo_pred(d, p, b0, idPV, acc ? 1u : 0u);
 #pragma unroll
-      for (int kk = 1; kk < KB / 16; ++kk)
-        if (kk < nk) tc::mma_ts_lo<1>(d, p + kk * 8, b0 + (uint32_t)((kk * 2048) >> 4), idPV);
+      for (int kk = 1; kk < KB / 16; ++kk) {
+        // a 16-key step: 16 rows of the MN-major tile, or 32 bytes along the K-major rows
+        const uint32_t off16 = KV8 ? ((kk / 4) * kBoxBytes + (kk % 4) * 32) >> 4
+                                   : (uint32_t)((kk * 2048) >> 4);
+        if (kk < nk) tc::mma_ts_lo<1>(d, p + kk * 8, b0 + off16, idPV);
+      }
     };
     uint32_t it = 0, sc = 0;
     int nitem = 0;
@@ -456,7 +710,7 @@ k_prefill(AttnArgs a, const __grid_constant__ AttnMaps maps) {
         if (kb + 1 == w.nkb && nvalid < KB) {
           nk = (nvalid + 15) / 16;
           const int n16 = (nk * 16 - nvalid) * 8;
-          if (qi == 0 && n16 > 0) {
+          if (!KV8 && qi == 0 && n16 > 0) {  // FP8 pages: cleared when widened
             for (int hf = 0; hf < Cfg::kHalves; ++hf) {
               uint4 *base = reinterpret_cast<uint4 *>(smem + Cfg::kV + st * Cfg::kTile +
                                                       hf * kBoxBytes + nvalid * 128);
@@ -813,7 +1067,7 @@ k_prefill(AttnArgs a, const __grid_constant__ AttnMaps maps) {
   }
 }
 
-template <int D, bool MASK>
+template <int D, bool MASK, bool KV8>
 static cudaError_t launch_prefill_t(const AttnArgs &a, int num_sms, const AttnMaps *maps,
                                     cudaStream_t s) {
   using Cfg = PfCfg<D>;
@@ -822,24 +1076,29 @@ static cudaError_t launch_prefill_t(const AttnArgs &a, int num_sms, const AttnMa
     // setmaxnreg.inc can only draw on registers the block was launched with: refuse to
     // launch (rather than wait forever) if the compiled allocation does not cover the split
     cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, k_prefill<D, MASK>);
+    cudaError_t e = cudaFuncGetAttributes(&fa, k_prefill<D, MASK, KV8>);
     if (e != cudaSuccess) return e;
     if (fa.numRegs * kPfThreads < kRegsSplitTotal) return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(k_prefill<D, MASK>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+    e = cudaFuncSetAttribute(k_prefill<D, MASK, KV8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg::kSmem);
     if (e != cudaSuccess) return e;
     setup.mark();
   }
-  k_prefill<D, MASK><<<num_sms, kPfThreads, Cfg::kSmem, s>>>(a, *maps);
+  k_prefill<D, MASK, KV8><<<num_sms, kPfThreads, Cfg::kSmem, s>>>(a, *maps);
   return cudaGetLastError();
 }
 
 cudaError_t launch_prefill(const AttnArgs &a, int num_sms, const void *tmaps, cudaStream_t s) {
   const AttnMaps *maps = static_cast<const AttnMaps *>(tmaps);
   const bool mask = a.cell_seq != nullptr;
-  if (a.D == 128) return mask ? launch_prefill_t<128, true>(a, num_sms, maps, s)
-                              : launch_prefill_t<128, false>(a, num_sms, maps, s);
-  if (a.D == 64) return mask ? launch_prefill_t<64, true>(a, num_sms, maps, s)
-                             : launch_prefill_t<64, false>(a, num_sms, maps, s);
+  if (a.k_scale) {  // FP8 pages: page size 128, d 128
+    if (a.D != 128 || a.P != KB || mask) return cudaErrorInvalidValue;
+    return launch_prefill_t<128, false, true>(a, num_sms, maps, s);
+  }
+  if (a.D == 128) return mask ? launch_prefill_t<128, true, false>(a, num_sms, maps, s)
+                              : launch_prefill_t<128, false, false>(a, num_sms, maps, s);
+  if (a.D == 64) return mask ? launch_prefill_t<64, true, false>(a, num_sms, maps, s)
+                             : launch_prefill_t<64, false, false>(a, num_sms, maps, s);
   return cudaErrorInvalidValue;
 }
 

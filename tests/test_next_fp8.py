@@ -231,3 +231,159 @@ def test_decode_fp8_is_bitwise_deterministic(pa):
     a, _ = _fp8_run(pa, case, pool, tpt, kv)
     b, _ = _fp8_run(pa, case, pool, tpt, kv)
     assert np.array_equal(a, b)
+
+
+# ------------------------------------------------------------------ GPU: prefill tiles over FP8
+
+def nan_fp8_pool(N, Hkv, P=128, d=128):
+    """A pool whose unwritten cells hold NaN codes (0x7F) and NaN scales: only the
+    cells below a token's kv_len may reach its output."""
+    return (np.full((N, Hkv, P, d), 0x7F, np.uint8), np.full((N, Hkv, d, P), 0x7F, np.uint8),
+            np.full((N, Hkv, P), np.nan, np.float32), np.full((N, Hkv, P), np.nan, np.float32))
+
+
+def unique_rows(case):
+    """Every cached row once (pages shared by several sequences are written once)."""
+    filled = np.zeros(case.num_pages * case.P, bool)
+    ks, vs, sl = [], [], []
+    for s, pages in enumerate(case.seq_pages):
+        L = int(case.seq_len[s])
+        pos = np.arange(L)
+        slots = np.asarray(pages, np.int64)[pos // case.P] * case.P + pos % case.P
+        new = ~filled[slots]
+        filled[slots] = True
+        sl.append(slots[new])
+        ks.append(case.k_ctx[s][:L][new])
+        vs.append(case.v_ctx[s][:L][new])
+    return np.concatenate(ks), np.concatenate(vs), np.concatenate(sl)
+
+
+def fp8_on_gpu(pa, case):
+    """Quantise every cached row into a NaN-filled FP8 pool, on the host (oracle) and on
+    the device (checked bit-exact); returns (oracle pool, device pool, tpt, kv)."""
+    k, v, slot = unique_rows(case)
+    ref = nan_fp8_pool(case.num_pages, case.Hkv)
+    oracle.kv_append_fp8(k, v, slot, *ref)
+    dev = "cuda"
+    pool = [torch.from_numpy(x).to(dev) for x in nan_fp8_pool(case.num_pages, case.Hkv)]
+    pa.kv_append_fp8(torch.from_numpy(k.view(np.float16)).to(dev),
+                     torch.from_numpy(v.view(np.float16)).to(dev),
+                     torch.from_numpy(slot).to(dev), *pool)
+    torch.cuda.synchronize()
+    for got, want in zip(pool, ref):
+        assert np.array_equal(got.cpu().numpy().view(np.uint8), want.view(np.uint8))
+    tpt, kv, _ = oracle.expand_ubatch(case.seq_page_table(), case.tok_seq, case.tok_pos, case.P)
+    return ref, pool, tpt, kv
+
+
+def run_forward_fp8(pa, case, pool, tpt, kv, min_run=16):
+    dev = "cuda"
+    old = pa.set_prefill_min_run(min_run)
+    try:
+        q = torch.from_numpy(case.q.view(np.float16)).to(dev)
+        out = torch.full_like(q, float("nan"))
+        ws = pa.new_workspace(case.T, case.Hq, case.Hkv, 128, dev)
+        pa.forward_fp8(q, *pool, torch.from_numpy(tpt).to(dev), torch.from_numpy(kv).to(dev),
+                       case.scale, out=out, workspace=ws)
+        torch.cuda.synchronize()
+        return out.float().cpu().numpy(), pa.read_error(ws)
+    finally:
+        pa.set_prefill_min_run(old)
+
+
+def tiny128(seed=0):
+    """The tiny workload's sequences and tokens (lengths 37 and 100; tokens 32..36 of
+    the first, 97..99 of the second) at the page size and head dimension FP8 pages
+    support (128, 128)."""
+    tokens = [(0, p) for p in range(32, 37)] + [(1, p) for p in range(97, 100)]
+    return workloads.build_case("tiny128", seed, [37, 100], tokens, P=128, Hq=4, Hkv=2, d=128,
+                                num_pages=8, scale=1.0 / np.sqrt(128.0))
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("min_run", [1, 16, 1 << 30], ids=["all_prefill", "default", "all_decode"])
+def test_forward_fp8_tiny(pa, min_run):
+    from tests._gpu import assert_attn_close
+    case = tiny128(0)
+    ref, pool, tpt, kv = fp8_on_gpu(pa, case)
+    want = oracle.paged_attention_fp8(case.q, *ref, tpt, kv, case.scale)
+    got, err = run_forward_fp8(pa, case, pool, tpt, kv, min_run)
+    assert err == 0
+    assert_attn_close(got, want, "fp8 tiny128")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("Hq,Hkv", [(8, 2), (32, 8), (8, 8)])
+@pytest.mark.parametrize("min_run", [1, 16], ids=["all_prefill", "default"])
+def test_forward_fp8_small_mixed(pa, Hq, Hkv, min_run):
+    from tests._gpu import assert_attn_close
+    case = workloads.small_prefill(5, P=128, d=128, Hq=Hq, Hkv=Hkv)
+    ref, pool, tpt, kv = fp8_on_gpu(pa, case)
+    want = oracle.paged_attention_fp8(case.q, *ref, tpt, kv, case.scale)
+    got, err = run_forward_fp8(pa, case, pool, tpt, kv, min_run)
+    assert err == 0
+    assert_attn_close(got, want, f"fp8 small mixed {Hq}/{Hkv}")
+
+
+@pytest.mark.gpu
+def test_forward_fp8_long_chunks_split_items(pa):
+    """Chunks of several key blocks: items are cut across CTAs (stream-K parts,
+    combined by the last one) and tiles end on ragged key counts."""
+    from tests._gpu import assert_attn_close
+    case = workloads.small_prefill(6, P=128, d=128, Hq=32, Hkv=8,
+                                   chunks=((0, 2000, 700), (1, 0, 300), (2, 5000, 129)),
+                                   extra_decode=3)
+    ref, pool, tpt, kv = fp8_on_gpu(pa, case)
+    rng = np.random.default_rng(7)
+    toks = sorted(set(rng.choice(case.T, 96, replace=False).tolist()) | {0, case.T - 1})
+    want = oracle.paged_attention_fp8(case.q, *ref, tpt, kv, case.scale, tokens=toks)
+    got, err = run_forward_fp8(pa, case, pool, tpt, kv, 16)
+    assert err == 0
+    assert np.all(np.isfinite(got))
+    assert_attn_close(got[toks], want, "fp8 long chunks")
+
+
+@pytest.mark.gpu
+def test_forward_fp8_shared_prefix(pa):
+    from tests._gpu import assert_attn_close
+    case = workloads.shared_prefix(0)
+    ref, pool, tpt, kv = fp8_on_gpu(pa, case)
+    rng = np.random.default_rng(2)
+    pre = rng.choice(np.arange(12, case.T), 24, replace=False).tolist()
+    toks = list(range(12)) + sorted(pre) + [case.T - 1]
+    want = oracle.paged_attention_fp8(case.q, *ref, tpt, kv, case.scale, tokens=toks)
+    got, err = run_forward_fp8(pa, case, pool, tpt, kv, 16)
+    assert err == 0
+    assert np.all(np.isfinite(got))
+    assert_attn_close(got[toks], want, "fp8 shared prefix")
+
+
+@pytest.mark.gpu
+def test_prefill_fp8_bad_page_and_repeat(pa):
+    case = workloads.small_prefill(8, P=128, d=128, Hq=8, Hkv=2)
+    ref, pool, tpt, kv = fp8_on_gpu(pa, case)
+    a, err_a = run_forward_fp8(pa, case, pool, tpt, kv, 1)
+    b, err_b = run_forward_fp8(pa, case, pool, tpt, kv, 1)
+    assert err_a == 0 and err_b == 0
+    assert np.array_equal(a, b)  # bitwise deterministic
+    bad = tpt.copy()
+    bad[0, 0] = case.num_pages + 5  # a prefill tile's first page is out of the pool
+    c, err_c = run_forward_fp8(pa, case, pool, bad, kv, 1)
+    assert err_c & pa.PA_ERR_PAGE_RANGE
+    # the context stays usable
+    d_, err_d = run_forward_fp8(pa, case, pool, tpt, kv, 1)
+    assert err_d == 0 and np.array_equal(a, d_)
+
+
+@pytest.mark.gpu
+def test_prefill_fp8_refuses_other_shapes(pa):
+    case = workloads.tiny(0)  # page size 16, d 64
+    dev = "cuda"
+    N = case.num_pages
+    pool = [torch.from_numpy(x).to(dev) for x in nan_fp8_pool(N, case.Hkv, case.P, case.d)]
+    tpt, kv, _ = oracle.expand_ubatch(case.seq_page_table(), case.tok_seq, case.tok_pos, case.P)
+    q = torch.from_numpy(case.q.view(np.float16)).to(dev)
+    with pytest.raises(pa.PagedAttnError) as e:
+        pa.forward_fp8(q, *pool, torch.from_numpy(tpt).to(dev), torch.from_numpy(kv).to(dev),
+                       case.scale)
+    assert e.value.status == pa.PA_EUNSUPPORTED
