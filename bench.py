@@ -451,7 +451,7 @@ def cpu_baseline_prefill(wl, budget_s=12.0, keep=False):
     kept = []
     while secs < budget_s and i < len(mids):
         u = mids[i]
-        q = d["q"].cpu().numpy().view(np.uint16)
+        ts, tp, q, _, _ = wl.ubatch(u)
         tpt, kv, _ = oracle.expand_ubatch(wl.seq_page_table, ts, tp, wl.P)
         sel = np.arange(0, ts.shape[0], stride, dtype=np.int32)
         t0 = time.perf_counter()
@@ -770,7 +770,7 @@ def bench_fp8_prefill(pa, torch, pb, steps, warmup, world, peak, f16_ms_per_step
         import oracle
         u = n_ub - 1
         d = pb.ub[u]
-        ts, tp, q, _, _ = wl.ubatch(u)
+        q = d["q"].cpu().numpy().view(np.uint16)
         rng = np.random.default_rng(11)
         sel = np.sort(rng.choice(d["T"], min(24, d["T"]), replace=False)).astype(np.int32)
         host = [x.cpu().numpy() for x in pool]

@@ -55,7 +55,7 @@ constexpr int kWarpMma = 9;
 constexpr int kBoxBytes = 128 * 128;  // 128 rows x 64 halves
 constexpr float kRescaleThreshold = 8.0f;
 
-template <int D>
+template <int D, bool KV8 = false>
 struct PfCfg {
   static constexpr int kHalves = D / 64;
   static constexpr int kTile = kHalves * kBoxBytes;  // 128 rows x D halves
@@ -63,13 +63,19 @@ struct PfCfg {
   static constexpr int kQ1 = kTile;
   static constexpr int kK = 2 * kTile;
   static constexpr int kV = kK + kPfStages * kTile;
-  static constexpr int kBarOff = kV + kPfStages * kTile;
+  // FP8 pages: the codes of the next K block and of the next V block wait here
+  static constexpr int kStgK = kV + kPfStages * kTile;
+  static constexpr int kStgV = kStgK + (KV8 ? kBoxBytes : 0);
+  static constexpr int kBarOff = kStgV + (KV8 ? kBoxBytes : 0);
   // masked variant: (sequence, position) of each key of the block, per softmax
-  // warpgroup, two buffers
+  // warpgroup, two buffers; FP8 pages: the V scales of each stage's block (binary32),
+  // then the K widening's scale table (binary16 hi and lo of each row)
   static constexpr int kCinfo = kBarOff + 256;
-  static constexpr int kUsed = kCinfo + 2 * 2 * 128 * 8;
+  static constexpr int kKtab = kCinfo + kPfStages * 128 * 4;
+  static constexpr int kUsed = KV8 ? kKtab + 128 * 4 : kCinfo + 2 * 2 * 128 * 8;
   // at least ~120 KB so that a second CTA never shares the SM (and its TMEM)
   static constexpr int kSmem = (kUsed < 120 * 1024 ? 120 * 1024 : kUsed) + 1024;
+  static_assert(kSmem <= 227 * 1024, "shared memory of one CTA");
 };
 
 struct PfBars {
@@ -77,7 +83,9 @@ struct PfBars {
   uint64_t k_full[kPfStages], k_empty[kPfStages], v_full[kPfStages], v_empty[kPfStages];
   uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
   uint64_t turn[2];  // issuer turns: tile 1's issuer -> tile 0's, tile 0's -> tile 1's
-  uint64_t kc_full, vc_full;  // FP8 pages: a block's codes have landed (K, V)
+  // FP8 pages: a block's codes have landed (K, V); the V scales of the stage's block are in
+  uint64_t kc_full, vc_full;
+  uint64_t vs_full[kPfStages];
   uint32_t tmem_base;
   int abort;
 };
@@ -99,32 +107,25 @@ __device__ __forceinline__ bool pf_wait(uint64_t *bar, uint32_t parity, int *err
 }
 
 // ---- FP8 pages: E4M3 codes widened to binary16 in shared memory -----------------
-// A block's codes (128 rows x 128 bytes, the 128-byte swizzle) land in the upper half
-// of the stage's binary16 tile and are widened in place: row r of the codes sits where
-// row r of the tile's second 64-column box goes, so each row is read whole before any
-// of it is written.  Lane = (row r = 4i + lane / 8, 16-code chunk c = lane % 8): a
-// quarter-warp covers one row, and its loads and stores hit eight distinct 16-byte
-// bank groups.  Each element becomes binary16(code * scale): the exact E4M3 value
-// (cvt), times the scale split in two binary16 parts (hi = rn(s), lo = rn(s - hi)),
+// A block's codes (128 rows x 128 bytes, the 128-byte swizzle) land in a staging buffer
+// one block ahead and are widened into the stage's binary16 tile once the stage is free.
+// K: each element becomes binary16(code * scale of its key): the exact E4M3 value (cvt),
+// times the scale split in two binary16 parts (hi = rn(s), lo = rn(s - hi)),
 // x * hi + x * lo, so the result is the binary16 rounding of code * scale up to the
-// rounding of the small x * lo term.
+// rounding of the small x * lo term.  V: the exact E4M3 values; each key's scale goes
+// into P instead (the softmax stores binary16(p * scale)), as in the split-KV decode.
 
-// the scale s as hi = rn(s) and lo = rn(s - hi), both binary16
-__device__ __forceinline__ void scale_split(float s, __half &hi, __half &lo) {
-  hi = __float2half_rn(s);
-  lo = __float2half_rn(s - __half2float(hi));
-}
-
-__device__ __forceinline__ uint32_t h2_bits(__half a, __half b) {
-  const __half2 h = __halves2half2(a, b);
+// (hi, lo) of the scale s packed in one word: hi = rn(s), lo = rn(s - hi), binary16
+__device__ __forceinline__ uint32_t scale_hl(float s) {
+  const __half hi = __float2half_rn(s);
+  const __half lo = __float2half_rn(s - __half2float(hi));
+  const __half2 h = __halves2half2(hi, lo);
   return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-// (hi, hi) and (lo, lo) of one scale, packed
-__device__ __forceinline__ uint2 scale_h2(float s) {
-  __half hi, lo;
-  scale_split(s, hi, lo);
-  return make_uint2(h2_bits(hi, hi), h2_bits(lo, lo));
+// (hi, hi) and (lo, lo) from a packed (hi, lo)
+__device__ __forceinline__ uint2 hl_pairs(uint32_t hl) {
+  return make_uint2(__byte_perm(hl, 0, 0x1010), __byte_perm(hl, 0, 0x3232));
 }
 
 // four E4M3 codes (byte i = element i) -> two binary16 pairs, exact
@@ -142,46 +143,64 @@ __device__ __forceinline__ uint32_t h2_scale(uint32_t x, uint32_t hi, uint32_t l
   return r;
 }
 
-// Widen the 128 x 128 codes at tile + kBoxBytes into the binary16 tile (two boxes of
-// 128 rows x 64 columns).  ROW: one scale per row (K: rows are keys), scales by row
-// from rtab[r] = (hi2, lo2); else one per column (V transposed: columns are keys), the
-// lane's 16 columns' pairs in chi/clo and codes of columns past the valid keys cleared
-// by cmask (an E4M3 NaN code times a zero scale would still be NaN).
-template <bool ROW>
-__device__ __forceinline__ void widen_tile(unsigned char *tile, const uint2 *rtab,
-                                           const uint32_t (&chi)[8], const uint32_t (&clo)[8],
-                                           const uint32_t (&cmask)[4], int lane) {
-  const int c = lane & 7, rs = lane >> 3;
-  const unsigned char *codes = tile + kBoxBytes;
-  unsigned char *box = tile + (c >> 2) * kBoxBytes;
-  // output chunks 2(c % 4) and 2(c % 4) + 1 of the row; lanes c < 4 store the even one
-  // first and lanes c >= 4 the odd one, so that a quarter-warp's stores never collide
-  const int first = 2 * (c & 3) + (c >> 2), second = first ^ 1;
+// 16 codes (one 16-byte chunk) -> 16 binary16 values in two 16-byte chunks, scaled by
+// rs = (hi2, lo2) if SCALE; with CLR the codes are first masked by cmask.
+template <bool SCALE, bool CLR>
+__device__ __forceinline__ void widen_chunk(uint4 x, uint2 rs, const uint32_t (&cmask)[4],
+                                            uint4 &o0, uint4 &o1) {
+  const uint32_t wd[4] = {CLR ? x.x & cmask[0] : x.x, CLR ? x.y & cmask[1] : x.y,
+                          CLR ? x.z & cmask[2] : x.z, CLR ? x.w & cmask[3] : x.w};
+  uint32_t h[8];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    uint32_t p01, p23;
+    e4m3x4_widen(wd[e], p01, p23);
+    h[2 * e] = SCALE ? h2_scale(p01, rs.x, rs.y) : p01;
+    h[2 * e + 1] = SCALE ? h2_scale(p23, rs.x, rs.y) : p23;
+  }
+  o0 = make_uint4(h[0], h[1], h[2], h[3]);
+  o1 = make_uint4(h[4], h[5], h[6], h[7]);
+}
+
+// Widen rows [4 i0, 4 i1) of the 128 x 128 codes at stg (rows of 128 bytes, the 128-byte
+// swizzle) into the binary16 tile (two boxes of 128 rows x 64 columns, the same swizzle).
+// K (SCALE): one scale per row, packed (hi, lo) in rtab[row].  V (no SCALE): with CLR the
+// codes of columns past the valid keys are cleared by cmask (they may be NaN codes).
+// Iteration i covers rows 4i..4i+3 as two row pairs {R, R + 1}; lane (quarter-warp q,
+// j = lane % 8) converts code chunk j of row R + ((q & 1) ^ (j / 4)) of pair q / 2, so a
+// quarter-warp reads chunks 0-3 of one row of its pair and 4-7 of the other, and stores
+// the even output chunk of each first: every 16-byte access of a quarter-warp lands in a
+// distinct bank group, and no lane needs a select.
+template <bool SCALE, bool CLR>
+__device__ __forceinline__ void widen_tile(const unsigned char *stg, unsigned char *tile,
+                                           const uint32_t *rtab, const uint32_t (&cmask)[4],
+                                           int lane, int i0, int i1) {
+  const int q = lane >> 3, j = lane & 7;
+  const int r0 = 2 * (q >> 1) + ((q & 1) ^ (j >> 2));  // row in iterations' first group
+  // row & 7 = r0 + 4 (i & 1): the swizzle phase of even and odd iterations
+  const int ch = 2 * (j & 3);  // output chunks ch, ch + 1 of box j / 4
+  const uint32_t ld_e = r0 * 128 + ((j ^ r0) << 4), ld_o = r0 * 128 + ((j ^ r0 ^ 4) << 4) + 512;
+  const uint32_t s0_e = r0 * 128 + ((ch ^ r0) << 4), s1_e = r0 * 128 + (((ch + 1) ^ r0) << 4);
+  const uint32_t s0_o = r0 * 128 + ((ch ^ r0 ^ 4) << 4) + 512,
+                 s1_o = r0 * 128 + (((ch + 1) ^ r0 ^ 4) << 4) + 512;
+  unsigned char *box = tile + (j >> 2) * kBoxBytes;
 #pragma unroll 1
-  for (int i = 0; i < 32; ++i) {
-    const int r = 4 * i + rs, sw = r & 7;
-    uint4 x = *reinterpret_cast<const uint4 *>(codes + r * 128 + ((c ^ sw) << 4));
-    uint32_t hi[4], lo[4];
-    if (ROW) {
-      const uint2 t = rtab[r];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) { hi[e] = t.x; lo[e] = t.y; }
+  for (int i = i0; i < i1; i += 2) {
+    const uint32_t base = (uint32_t)i * 512;
+    const uint4 xe = *reinterpret_cast<const uint4 *>(stg + base + ld_e);
+    const uint4 xo = *reinterpret_cast<const uint4 *>(stg + base + ld_o);
+    uint2 re = make_uint2(0, 0), ro = re;
+    if (SCALE) {  // rows 4i + r0 and 4i + 4 + r0
+      re = hl_pairs(rtab[4 * i + r0]);
+      ro = hl_pairs(rtab[4 * i + 4 + r0]);
     }
-    __syncwarp();  // the whole row is read before the second box's row overwrites it
-    const uint32_t wd[4] = {x.x & cmask[0], x.y & cmask[1], x.z & cmask[2], x.w & cmask[3]};
-    uint32_t h[8];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      uint32_t p01, p23;
-      e4m3x4_widen(wd[e], p01, p23);
-      h[2 * e] = ROW ? h2_scale(p01, hi[0], lo[0]) : h2_scale(p01, chi[2 * e], clo[2 * e]);
-      h[2 * e + 1] =
-          ROW ? h2_scale(p23, hi[0], lo[0]) : h2_scale(p23, chi[2 * e + 1], clo[2 * e + 1]);
-    }
-    const uint4 o0 = make_uint4(h[0], h[1], h[2], h[3]), o1 = make_uint4(h[4], h[5], h[6], h[7]);
-    unsigned char *rowp = box + r * 128;
-    *reinterpret_cast<uint4 *>(rowp + ((first ^ sw) << 4)) = (c >> 2) ? o1 : o0;
-    *reinterpret_cast<uint4 *>(rowp + ((second ^ sw) << 4)) = (c >> 2) ? o0 : o1;
+    uint4 a0, a1, b0, b1;
+    widen_chunk<SCALE, CLR>(xe, re, cmask, a0, a1);
+    widen_chunk<SCALE, CLR>(xo, ro, cmask, b0, b1);
+    *reinterpret_cast<uint4 *>(box + base + s0_e) = a0;
+    *reinterpret_cast<uint4 *>(box + base + s1_e) = a1;
+    *reinterpret_cast<uint4 *>(box + base + s0_o) = b0;
+    *reinterpret_cast<uint4 *>(box + base + s1_o) = b1;
   }
 }
 
@@ -324,6 +343,158 @@ __device__ __forceinline__ bool seg_first(Seg &s, const SegCtx &x, const PfWork 
   return seg_begin(s, x, pw.start, pw.w0, pw.w1);
 }
 
+// FP8 pages: the staging and widening of one tensor's codes, whole warp (ISK: K, warp
+// 8, which also loads the Q tiles; else V, warp 11).  Each warp stages its tensor's
+// codes one block ahead: block n + 1 is copied (one TMA box into the staging buffer) as
+// soon as block n has been widened out of it, and the block after that is asked into
+// L2.  K rows are widened with their scales; V rows keep the exact E4M3 values and the
+// warp hands the block's V scales to the softmax, which folds them into P.
+template <bool ISK>
+__device__ __forceinline__ void kv8_widen_role(const AttnArgs &a, const AttnMaps &maps,
+                                               PfBars *bars, unsigned char *smem, int *err,
+                                               volatile int *abort, int lane, int NQ, int NP,
+                                               int G) {
+  using Cfg = PfCfg<128, true>;
+  const PfWork pw = pf_work(a, NP, G);
+  const SegCtx &sx = pw.sx;
+  const float *scales = ISK ? a.k_scale : a.v_scale;
+  const CUtensorMap *map = ISK ? &maps.k : &maps.v;
+  uint64_t *cfull = ISK ? &bars->kc_full : &bars->vc_full;
+  uint64_t *tfull = ISK ? bars->k_full : bars->v_full;
+  uint64_t *tempty = ISK ? bars->k_empty : bars->v_empty;
+  unsigned char *stg = smem + (ISK ? Cfg::kStgK : Cfg::kStgV);
+  unsigned char *tiles = smem + (ISK ? Cfg::kK : Cfg::kV);
+  float *vsc = reinterpret_cast<float *>(smem + Cfg::kCinfo);  // V scales, per stage
+  uint32_t *ktab = reinterpret_cast<uint32_t *>(smem + Cfg::kKtab);  // K rows' (hi, lo)
+  const int c8 = lane & 7;
+  // rows of one (page, head) block in the code maps (K keys, V dims: both 128); the
+  // first row past the pool reads zeros
+  const int oob_row = a.num_pages * a.Hkv * KB;
+  Seg w{};
+  bool more = seg_first(w, sx, pw);
+  int kb = more ? w.kb_b : 0;
+  // (page, head) index of block x of the current item's rows, -1 for a missing page
+  auto block_of = [&](int x) -> int {
+    const int page = a.tpt[(size_t)w.tile_start * a.max_pages + x];
+    return page >= 0 && page < a.num_pages ? page * a.Hkv + w.g : -1;
+  };
+  // stage the codes of block (w, kb), (page, head) hp
+  auto stage = [&](int hp) {
+    if (lane != 0) return;
+    if (ISK && hp < 0) atomicOr(err, PA_ERR_PAGE_RANGE);
+    mbar_arrive_expect_tx(cfull, kBoxBytes);
+    tc::tma_load_2d(stg, map, 0, hp >= 0 ? hp * KB : oob_row, cfull);
+    if (kb + 1 < w.kb_e) {
+      const int hn = block_of(kb + 1);
+      if (hn >= 0) tc::tma_prefetch_2d(map, 0, hn * KB);
+    }
+    if (ISK && kb == w.kb_b)  // the item's Q tiles into L2 ahead of their load
+      for (int hf = 0; hf < Cfg::kHalves; ++hf) {
+        tc::tma_prefetch_3d(&maps.q, hf * 64, w.h0, w.tile_start);
+        if (NQ == 2) tc::tma_prefetch_3d(&maps.q, hf * 64, w.h1, w.tile_start);
+      }
+  };
+  // scales of keys 4 lane .. 4 lane + 3 of (page, head) hp; a missing page: zero scales
+  // (and zero codes: the box is past the pool)
+  auto load_scales = [&](int hp) -> float4 {
+    return hp >= 0 ? __ldg(reinterpret_cast<const float4 *>(scales + (size_t)hp * KB) + lane)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+  };
+  auto load_q = [&](int ts, int h0, int h1) {
+    mbar_arrive_expect_tx(&bars->q_full, NQ * Cfg::kTile);
+    for (int hf = 0; hf < Cfg::kHalves; ++hf) {
+      tc::tma_load_3d(smem + Cfg::kQ0 + hf * kBoxBytes, &maps.q, hf * 64, h0, ts, &bars->q_full);
+      if (NQ == 2)
+        tc::tma_load_3d(smem + Cfg::kQ1 + hf * kBoxBytes, &maps.q, hf * 64, h1, ts, &bars->q_full);
+    }
+  };
+  if (!more) return;
+  // the current block: item, key count, scales
+  int first, ts, h0, h1, nvalid;
+  float4 s4;
+  auto take = [&]() {  // (w, kb) becomes the current block; step (w, kb) to the next
+    first = kb == w.kb_b;
+    ts = w.tile_start;
+    h0 = w.h0;
+    h1 = w.h1;
+    nvalid = min(KB, w.max_kv - kb * KB);
+    if (++kb >= w.kb_e) {
+      more = seg_next(w, sx);
+      kb = more ? w.kb_b : 0;
+    }
+  };
+  {
+    const int hp = block_of(kb);
+    s4 = load_scales(hp);
+    if (ISK && lane == 0) load_q(w.tile_start, w.h0, w.h1);
+    stage(hp);
+    take();
+  }
+  uint32_t it = 0;
+  int nitem = 0;
+  for (;;) {
+    const int st = it % kPfStages;
+    const uint32_t ph = (it / kPfStages) & 1u;
+    // the next block's (page, head) and scales, in flight during this block's widening
+    const int nhp = more ? block_of(kb) : -1;
+    const float4 s4n = more ? load_scales(nhp) : make_float4(0.f, 0.f, 0.f, 0.f);
+    uint32_t cmask[4] = {~0u, ~0u, ~0u, ~0u};
+    if (ISK) {
+      __syncwarp();  // the previous block's table reads are done
+      reinterpret_cast<uint4 *>(ktab)[lane] =
+          make_uint4(scale_hl(s4.x), scale_hl(s4.y), scale_hl(s4.z), scale_hl(s4.w));
+      __syncwarp();
+    } else {
+      // keys past the tile's longest kv_len: cleared codes (they may be NaN codes: P is 0
+      // there, but 0 * NaN is NaN) and a zero scale
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int nb = min(max(nvalid - (16 * c8 + 4 * q), 0), 4);  // valid codes of the word
+        cmask[q] = nb >= 4 ? ~0u : (1u << (8 * nb)) - 1u;
+      }
+    }
+    if (!__all_sync(~0u, pf_wait(cfull, it & 1u, err, abort))) break;
+    if (!__all_sync(~0u, pf_wait(&tempty[st], ph ^ 1u, err, abort))) break;
+    unsigned char *tile = tiles + st * Cfg::kTile;
+    if (ISK) {
+      widen_tile<true, false>(stg, tile, ktab, cmask, lane, 0, 32);
+    } else {
+      // the block's V scales for the softmax (the stage's previous block is done with them)
+      float4 sc = s4;
+      if (4 * lane + 0 >= nvalid) sc.x = 0.f;
+      if (4 * lane + 1 >= nvalid) sc.y = 0.f;
+      if (4 * lane + 2 >= nvalid) sc.z = 0.f;
+      if (4 * lane + 3 >= nvalid) sc.w = 0.f;
+      reinterpret_cast<float4 *>(vsc + st * KB)[lane] = sc;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->vs_full[st]);
+      if (nvalid < KB)
+        widen_tile<false, true>(stg, tile, nullptr, cmask, lane, 0, 32);
+      else
+        widen_tile<false, false>(stg, tile, nullptr, cmask, lane, 0, 32);
+    }
+    // generic-proxy writes -> the tensor core's reads; the staging reads before the next
+    // block's copy overwrites it
+    fence_proxy_async();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&tfull[st]);
+    ++it;
+    if (more) stage(nhp);
+    if (ISK && first) {
+      // a new item: its Q tiles once the previous item's MMAs have released them
+      if (nitem > 0) {
+        if (!__all_sync(~0u, lane != 0 || pf_wait(&bars->q_empty, (nitem - 1) & 1, err, abort)))
+          break;
+        if (lane == 0) load_q(ts, h0, h1);
+      }
+      ++nitem;
+    }
+    if (!more) break;
+    s4 = s4n;
+    take();
+  }
+}
+
 // MASK: the unified-span baseline.  Every tile token's row names the same span of
 // cells; key j is kept only if its cell belongs to the token's sequence at a position
 // up to the token's own (cell_seq[slot] == tok_seq[t] && cell_pos[slot] <= tok_pos[t]),
@@ -339,7 +510,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 k_prefill(AttnArgs a, const __grid_constant__ AttnMaps maps) {
   static_assert(!(MASK && KV8), "one variant at a time");
   static_assert(!KV8 || D == 128, "FP8 pages: d 128");
-  using Cfg = PfCfg<D>;
+  using Cfg = PfCfg<D, KV8>;
   // rows of a split part's record: O[D] | m | l | 2 unused (D + 4 rows of 128 floats)
   constexpr int kPartStride = D + 4;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -382,6 +553,7 @@ k_prefill(AttnArgs a, const __grid_constant__ AttnMaps maps) {
     mbar_init(&bars->turn[1], 1);
     mbar_init(&bars->kc_full, 1);
     mbar_init(&bars->vc_full, 1);
+    for (int s = 0; s < kPfStages; ++s) mbar_init(&bars->vs_full[s], 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->p_full[i], 128);
@@ -410,154 +582,9 @@ k_prefill(AttnArgs a, const __grid_constant__ AttnMaps maps) {
   if (warp >= 8) {
    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
    if (KV8 && warp == kWarpTma) {
-    // ------------------------------------------------------------ FP8: Q, K codes (warp)
-    const PfWork pw = pf_work(a, NP, G);
-    const SegCtx &sx = pw.sx;
-    uint32_t it = 0;
-    int nitem = 0;
-    const int oob_row = a.num_pages * a.Hkv * KB;  // first row past the pool: zero fill
-    uint2 *ktab = reinterpret_cast<uint2 *>(smem + Cfg::kCinfo);
-    const uint32_t ones[4] = {~0u, ~0u, ~0u, ~0u};
-    const uint32_t none[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    Seg w{};
-    const int32_t *row = nullptr;
-    // K codes of key block kb (one page) into the upper half of stage it % kPfStages,
-    // widened there; the MMA issuers see k_full only once the binary16 tile is complete
-    auto k_block = [&](int kb) -> bool {
-      const int st = it % kPfStages;
-      const uint32_t ph = (it / kPfStages) & 1u;
-      if (!__all_sync(~0u, pf_wait(&bars->k_empty[st], ph ^ 1u, err, abort))) return false;
-      const int page = row[kb];
-      const bool pv = page >= 0 && page < a.num_pages;
-      const int r0 = pv ? (page * a.Hkv + w.g) * KB : oob_row;
-      unsigned char *tile = smem + Cfg::kK + st * Cfg::kTile;
-      if (lane == 0) {
-        if (!pv) atomicOr(err, PA_ERR_PAGE_RANGE);
-        mbar_arrive_expect_tx(&bars->kc_full, kBoxBytes);
-        tc::tma_load_2d(tile + kBoxBytes, &maps.k, 0, r0, &bars->kc_full);
-        if (kb + 1 < w.kb_e) {
-          const int pn = row[kb + 1];
-          if (pn >= 0 && pn < a.num_pages) tc::tma_prefetch_2d(&maps.k, 0, (pn * a.Hkv + w.g) * KB);
-        }
-      }
-      // row scales (a missing page: zero rows, zero scales) -> (hi, lo) table
-      const float4 s4 = pv ? __ldg(reinterpret_cast<const float4 *>(a.k_scale + r0) + lane)
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
-      const uint2 t0 = scale_h2(s4.x), t1 = scale_h2(s4.y), t2 = scale_h2(s4.z),
-                  t3 = scale_h2(s4.w);
-      __syncwarp();  // the previous block's table reads are done
-      reinterpret_cast<uint4 *>(ktab)[2 * lane] = make_uint4(t0.x, t0.y, t1.x, t1.y);
-      reinterpret_cast<uint4 *>(ktab)[2 * lane + 1] = make_uint4(t2.x, t2.y, t3.x, t3.y);
-      if (!__all_sync(~0u, pf_wait(&bars->kc_full, it & 1u, err, abort))) return false;
-      __syncwarp();
-      widen_tile<true>(tile, ktab, none, none, ones, lane);
-      fence_proxy_async();  // generic-proxy writes -> the tensor core's reads
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->k_full[st]);
-      ++it;
-      return true;
-    };
-    for (bool more = seg_first(w, sx, pw); more; more = seg_next(w, sx)) {
-      row = a.tpt + (size_t)w.tile_start * a.max_pages;
-      int kb = w.kb_b;
-      if (nitem > 0) {
-        if (!k_block(kb++)) break;
-        if (!__all_sync(~0u, lane != 0 || pf_wait(&bars->q_empty, (nitem - 1) & 1, err, abort)))
-          break;
-      }
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&bars->q_full, NQ * Cfg::kTile);
-        for (int hf = 0; hf < Cfg::kHalves; ++hf) {
-          tc::tma_load_3d(smem + Cfg::kQ0 + hf * kBoxBytes, &maps.q, hf * 64, w.h0, w.tile_start,
-                          &bars->q_full);
-          if (NQ == 2)
-            tc::tma_load_3d(smem + Cfg::kQ1 + hf * kBoxBytes, &maps.q, hf * 64, w.h1,
-                            w.tile_start, &bars->q_full);
-        }
-      }
-      bool ok = true;
-      for (; kb < w.kb_e && ok; ++kb) ok = k_block(kb);
-      if (!ok) break;
-      ++nitem;
-    }
+    kv8_widen_role<true>(a, maps, bars, smem, err, abort, lane, NQ, NP, G);
    } else if (KV8 && warp == kWarpTma + 3) {
-    // ------------------------------------------------------------ FP8: V codes (warp)
-    const PfWork pw = pf_work(a, NP, G);
-    const SegCtx &sx = pw.sx;
-    uint32_t it = 0;
-    const int oob_row = a.num_pages * a.Hkv * D;
-    uint32_t *vhi = reinterpret_cast<uint32_t *>(smem + Cfg::kCinfo + 1024);
-    uint32_t *vlo = vhi + KB / 2;
-    const int c8 = lane & 7;
-    Seg w{};
-    bool ok = true;
-    for (bool more = seg_first(w, sx, pw); more && ok; more = seg_next(w, sx)) {
-      const int32_t *row = a.tpt + (size_t)w.tile_start * a.max_pages;
-      for (int kb = w.kb_b; kb < w.kb_e; ++kb) {
-        const int st = it % kPfStages;
-        const uint32_t ph = (it / kPfStages) & 1u;
-        if (!__all_sync(~0u, pf_wait(&bars->v_empty[st], ph ^ 1u, err, abort))) {
-          ok = false;
-          break;
-        }
-        const int page = row[kb];
-        const bool pv = page >= 0 && page < a.num_pages;
-        const int hp = page * a.Hkv + w.g;
-        unsigned char *tile = smem + Cfg::kV + st * Cfg::kTile;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&bars->vc_full, kBoxBytes);
-          tc::tma_load_2d(tile + kBoxBytes, &maps.v, 0, pv ? hp * D : oob_row, &bars->vc_full);
-          if (kb + 1 < w.kb_e) {
-            const int pn = row[kb + 1];
-            if (pn >= 0 && pn < a.num_pages) tc::tma_prefetch_2d(&maps.v, 0, (pn * a.Hkv + w.g) * D);
-          }
-        }
-        // keys past the tile's longest kv_len: zero scale and cleared codes (they may
-        // hold anything, NaN codes included, and P is 0 there but 0 * NaN is NaN)
-        const int nvalid = min(KB, w.max_kv - kb * KB);
-        float4 s4 = pv ? __ldg(reinterpret_cast<const float4 *>(a.v_scale + (size_t)hp * KB) + lane)
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
-        if (4 * lane + 0 >= nvalid) s4.x = 0.f;
-        if (4 * lane + 1 >= nvalid) s4.y = 0.f;
-        if (4 * lane + 2 >= nvalid) s4.z = 0.f;
-        if (4 * lane + 3 >= nvalid) s4.w = 0.f;
-        __half h0, l0, h1, l1, h2, l2, h3, l3;
-        scale_split(s4.x, h0, l0);
-        scale_split(s4.y, h1, l1);
-        scale_split(s4.z, h2, l2);
-        scale_split(s4.w, h3, l3);
-        __syncwarp();  // the previous block's table reads are done
-        reinterpret_cast<uint2 *>(vhi)[lane] = make_uint2(h2_bits(h0, h1), h2_bits(h2, h3));
-        reinterpret_cast<uint2 *>(vlo)[lane] = make_uint2(h2_bits(l0, l1), h2_bits(l2, l3));
-        __syncwarp();
-        uint32_t chi[8], clo[8], cmask[4];
-        {
-          const uint4 a0 = reinterpret_cast<const uint4 *>(vhi)[2 * c8],
-                      a1 = reinterpret_cast<const uint4 *>(vhi)[2 * c8 + 1],
-                      b0 = reinterpret_cast<const uint4 *>(vlo)[2 * c8],
-                      b1 = reinterpret_cast<const uint4 *>(vlo)[2 * c8 + 1];
-          chi[0] = a0.x; chi[1] = a0.y; chi[2] = a0.z; chi[3] = a0.w;
-          chi[4] = a1.x; chi[5] = a1.y; chi[6] = a1.z; chi[7] = a1.w;
-          clo[0] = b0.x; clo[1] = b0.y; clo[2] = b0.z; clo[3] = b0.w;
-          clo[4] = b1.x; clo[5] = b1.y; clo[6] = b1.z; clo[7] = b1.w;
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int nb = min(max(nvalid - (16 * c8 + 4 * q), 0), 4);  // valid codes of the word
-          cmask[q] = nb >= 4 ? ~0u : (1u << (8 * nb)) - 1u;
-        }
-        if (!__all_sync(~0u, pf_wait(&bars->vc_full, it & 1u, err, abort))) {
-          ok = false;
-          break;
-        }
-        __syncwarp();
-        widen_tile<false>(tile, nullptr, chi, clo, cmask, lane);
-        fence_proxy_async();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->v_full[st]);
-        ++it;
-      }
-    }
+    kv8_widen_role<false>(a, maps, bars, smem, err, abort, lane, NQ, NP, G);
    } else if (!KV8 && warp == kWarpTma && lane == 0) {
     // ------------------------------------------------------------ TMA producer
     {
@@ -878,6 +905,15 @@ k_prefill(AttnArgs a, const __grid_constant__ AttnMaps maps) {
           const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
           const float2 nm2 = make_float2(-m_use, -m_use);
           float2 rs2 = make_float2(0.f, 0.f);
+          // FP8 pages: P carries each key's V scale (binary16(p * scale); the row sum l
+          // does not), so the V tile holds the exact E4M3 values
+          const float2 *vs2 = nullptr;
+          if (KV8) {
+            const uint32_t cur = sc + kk;
+            const int st = cur % kPfStages;
+            if (!pf_wait(&bars->vs_full[st], (cur / kPfStages) & 1u, err, abort)) { ok = false; break; }
+            vs2 = reinterpret_cast<const float2 *>(smem + Cfg::kCinfo) + st * (KB / 2);
+          }
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
             uint32_t pk[16];
@@ -886,8 +922,9 @@ k_prefill(AttnArgs a, const __grid_constant__ AttnMaps maps) {
               const int c = 32 * q4 + j;
               const float2 x =
                   ffma2(make_float2(__uint_as_float(t[c]), __uint_as_float(t[c + 1])), sc2, nm2);
-              const float2 p = make_float2(exp2_approx(x.x), exp2_approx(x.y));
+              float2 p = make_float2(exp2_approx(x.x), exp2_approx(x.y));
               rs2 = fadd2(rs2, p);
+              if (KV8) p = fmul2(p, vs2[c >> 1]);
               __half2 hp = __floats2half2_rn(p.x, p.y);
               pk[j >> 1] = *reinterpret_cast<uint32_t *>(&hp);
             }
@@ -1070,7 +1107,7 @@ k_prefill(AttnArgs a, const __grid_constant__ AttnMaps maps) {
 template <int D, bool MASK, bool KV8>
 static cudaError_t launch_prefill_t(const AttnArgs &a, int num_sms, const AttnMaps *maps,
                                     cudaStream_t s) {
-  using Cfg = PfCfg<D>;
+  using Cfg = PfCfg<D, KV8>;
   static PerDeviceOnce setup;
   if (setup.first()) {
     // setmaxnreg.inc can only draw on registers the block was launched with: refuse to

@@ -4,6 +4,9 @@
       one ubatch of the 8 x 16K prefill (default: a late one, long contexts):
       expand -> append -> plan -> prefill -> decode, R times.  Device memory:
       the 655 MB KV pool (larger than L2) plus one ubatch.
+  python -m paged_kv_cache_pages_gb300.profile_case prefill_fp8 [--ubatch U] [--reps R]
+      the same ubatch over FP8 pages (every row of the 8 sequences quantised by the
+      library's append: 336 MB of codes), the prefill call alone, R times.
   python -m paged_kv_cache_pages_gb300.profile_case decode [--reps R] [--pools N]
       the 8-sequence decode layer: expand -> plan -> append -> decode, over N
       copies of the 82 MB pool used in turn (default 8: 660 MB, larger than L2,
@@ -135,6 +138,37 @@ def span(reps: int):
           f"({c.num_pages} pages read by each of {c.T} tokens)")
 
 
+def prefill_fp8(ubatch: int, reps: int):
+    wl = workloads.Prefill8x16K(0)
+    K, V = wl._draw_kv()
+    dev = "cuda"
+    pos = np.arange(wl.seq_len)
+    slots = np.concatenate([wl.seq_page_table[s][pos // wl.P].astype(np.int64) * wl.P + pos % wl.P
+                            for s in range(wl.n_seq)])
+    pool = pa.new_fp8_pool(wl.num_pages, wl.Hkv, wl.P, wl.d, dev)
+    pa.kv_append_fp8(torch.from_numpy(K.reshape(-1, wl.Hkv, wl.d).view(np.float16)).to(dev),
+                     torch.from_numpy(V.reshape(-1, wl.Hkv, wl.d).view(np.float16)).to(dev),
+                     torch.from_numpy(slots).to(dev), *pool)
+    ts, tp, q, _, _ = wl.ubatch(ubatch)
+    spt = torch.from_numpy(wl.seq_page_table).to(dev)
+    q_d = torch.from_numpy(q.view(np.float16)).to(dev)
+    out = torch.empty_like(q_d)
+    ws = pa.new_workspace(ts.shape[0], wl.Hq, wl.Hkv, wl.d, dev)
+    tpt, kv, _ = pa.expand_ubatch(spt, torch.from_numpy(ts).to(dev), torch.from_numpy(tp).to(dev),
+                                  wl.P)
+    pa.plan(tpt, kv, wl.Hq, wl.Hkv, wl.P, wl.d, ws)
+
+    def fn():
+        pa.prefill_fp8(q_d, *pool, tpt, kv, wl.scale, out, ws)
+
+    ms = _time(fn, reps)
+    if pa.read_error(ws):
+        raise SystemExit("device error word set")
+    flops = 4.0 * wl.d * wl.Hq * float((tp.astype(np.int64) + 1).sum())
+    print(f"prefill_fp8 ubatch {ubatch}: T={ts.shape[0]} {ms * 1e3:.1f} us/call "
+          f"{flops / ms / 1e9:.1f} TFLOP/s (prefill call; FP8 pool of every row)")
+
+
 def fp8(reps: int, n_pools: int):
     c = workloads.decode(0)
     dev = "cuda"
@@ -187,13 +221,16 @@ def copy(reps: int):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["prefill", "decode", "longtail", "copy", "span", "fp8"])
+    ap.add_argument("case", choices=["prefill", "prefill_fp8", "decode", "longtail", "copy",
+                                     "span", "fp8"])
     ap.add_argument("--ubatch", type=int, default=48)
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--pools", type=int, default=8)
     a = ap.parse_args()
     if a.case == "prefill":
         prefill(a.ubatch, a.reps)
+    elif a.case == "prefill_fp8":
+        prefill_fp8(a.ubatch, a.reps)
     elif a.case == "decode":
         decode(a.reps, a.pools)
     elif a.case == "longtail":
