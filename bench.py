@@ -36,8 +36,8 @@ METRIC = "decode KV GB/s + prefill TFLOP/s, Qwen3-8B-shape paged attn, 8×16K, 1
 # --ubatch 48` / `prefill_fp8 --ubatch 48`, scaled to the 8x16K step's mean work per
 # launch (16,258 of ubatch 48's 16,640 key-block units); k_decode: one decode_8seq
 # launch (`profile_case decode`); k_decode_longtail: `profile_case longtail`;
-# k_decode_span: one masked launch of `profile_case span`; k_decode_fp8: one FP8 launch
-# of `profile_case fp8`; k_copy_pages: one launch of `profile_case copy` (writes still
+# k_decode_span: one masked launch of `profile_case span`; k_decode_fp8 /
+# k_decode_fp8_longtail: one FP8 launch of `profile_case fp8` / `fp8_longtail`; k_copy_pages: one launch of `profile_case copy` (writes still
 # in L2 at the end of the launch are not counted).  Summaries and commands: profiles/.
 TRAFFIC = {
     "k_prefill": {"bytes": 399.25e6, "files": ["k_prefill.cu"], "digest": "81914d0bdbb4fc41"},
@@ -46,6 +46,7 @@ TRAFFIC = {
     "k_decode_longtail": {"bytes": 1082.34e6, "files": ["k_decode.cu"], "digest": "09be4cb3b3b619e0"},
     "k_decode_span": {"bytes": 116.64e6, "files": ["k_decode.cu"], "digest": "09be4cb3b3b619e0"},
     "k_decode_fp8": {"bytes": 43.69e6, "files": ["k_decode.cu"], "digest": "09be4cb3b3b619e0"},
+    "k_decode_fp8_longtail": {"bytes": 559.81e6, "files": ["k_decode.cu"], "digest": "09be4cb3b3b619e0"},
     "k_copy_pages": {"bytes": 488.04e6, "files": ["k_small.cu"], "digest": "8ffc91b37d609dbd"},
 }
 _TRAFFIC_HEADERS = ["common.cuh", "tc.cuh", "tmap.cuh", "kernels.cuh"]

@@ -22,6 +22,9 @@
   python -m paged_kv_cache_pages_gb300.profile_case fp8 [--reps R] [--pools N]
       the decode layer over FP8 pages (every cached row quantised by the
       library's append), N pool copies in turn (default 8).
+  python -m paged_kv_cache_pages_gb300.profile_case fp8_longtail [--reps R] [--pools N]
+      the long-tail layer over FP8 pages (0.55 GB of codes and scales), N copies in
+      turn (use 2).
   python -m paged_kv_cache_pages_gb300.profile_case copy [--reps R]
       page copy of copy-on-write forks: 512 of 1280 pages (8 KV heads x 128 rows
       x d 128, K and V) copied to 512 others per call.
@@ -169,8 +172,8 @@ def prefill_fp8(ubatch: int, reps: int):
           f"{flops / ms / 1e9:.1f} TFLOP/s (prefill call; FP8 pool of every row)")
 
 
-def fp8(reps: int, n_pools: int):
-    c = workloads.decode(0)
+def fp8(reps: int, n_pools: int, longtail: bool = False):
+    c = workloads.longtail(0) if longtail else workloads.decode(0)
     dev = "cuda"
     tpt, kv, _ = pa.expand_ubatch(
         torch.from_numpy(c.seq_page_table()).to(dev), torch.from_numpy(c.tok_seq).to(dev),
@@ -202,7 +205,8 @@ def fp8(reps: int, n_pools: int):
     if pa.read_error(ws):
         raise SystemExit("device error word set")
     nbytes = float(c.seq_len.astype(np.int64).sum()) * c.Hkv * (2 * c.d + 8)
-    print(f"fp8: {ms * 1e3:.1f} us/call {nbytes / ms / 1e6:.1f} GB/s ({len(pools)} pools in turn)")
+    print(f"fp8 {c.name}: {ms * 1e3:.1f} us/call {nbytes / ms / 1e6:.1f} GB/s "
+          f"({len(pools)} pools in turn)")
 
 
 def copy(reps: int):
@@ -222,7 +226,7 @@ def copy(reps: int):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("case", choices=["prefill", "prefill_fp8", "decode", "longtail", "copy",
-                                     "span", "fp8"])
+                                     "span", "fp8", "fp8_longtail"])
     ap.add_argument("--ubatch", type=int, default=48)
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--pools", type=int, default=8)
@@ -239,6 +243,8 @@ def main():
         span(a.reps)
     elif a.case == "fp8":
         fp8(a.reps, a.pools)
+    elif a.case == "fp8_longtail":
+        fp8(a.reps, a.pools, longtail=True)
     else:
         copy(a.reps)
 
