@@ -22,8 +22,9 @@
  *              pa_pool_* (host page pool)
  *  beyond it:  paged_attn_plan_decode, paged_attn_plan_prefill;
  *              paged_attn_masked_decode and paged_attn_masked_prefill (the
- *              unified-span baseline that paging replaces); paged_kv_append_fp8
- *              and paged_attn_decode_fp8 (FP8 pages); paged_copy_pages and
+ *              unified-span baseline that paging replaces); paged_kv_append_fp8,
+ *              paged_attn_decode_fp8, paged_attn_prefill_fp8 and
+ *              paged_attn_forward_fp8 (FP8 pages); paged_copy_pages and
  *              pa_pool_fork (copy-on-write forks of shared pages)
  *
  * Conventions shared by every call
