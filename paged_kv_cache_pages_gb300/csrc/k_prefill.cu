@@ -184,7 +184,7 @@ __device__ __forceinline__ void widen_tile(const unsigned char *stg, unsigned ch
   const uint32_t s0_o = r0 * 128 + ((ch ^ r0 ^ 4) << 4) + 512,
                  s1_o = r0 * 128 + (((ch + 1) ^ r0 ^ 4) << 4) + 512;
   unsigned char *box = tile + (j >> 2) * kBoxBytes;
-#pragma unroll 1
+#pragma unroll 2
   for (int i = i0; i < i1; i += 2) {
     const uint32_t base = (uint32_t)i * 512;
     const uint4 xe = *reinterpret_cast<const uint4 *>(stg + base + ld_e);
