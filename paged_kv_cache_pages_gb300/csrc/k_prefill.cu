@@ -1025,60 +1025,115 @@ k_prefill(AttnArgs a, const __grid_constant__ AttnMaps maps) {
           old = __shfl_sync(0xffffffffu, old, 0);
           if (old == n_parts - 1) {
             __threadfence();
-            // The other parts were written by other SMs: read them past L1 (ld.global.cg).
-            // This CTA's own part is still in registers.  Parts are folded in CTA order
-            // with the same arithmetic whichever CTA combines, so results are reproducible.
+            // Parts are folded in CTA order with the same arithmetic whichever CTA
+            // combines, so results are reproducible.  The other parts were written by
+            // other SMs: read them past L1 (ld.global.cg).
             auto slot_of = [&](int cc) {
               return 2 * cc + (w.item_start <= (long long)cc * W / C ? 0 : 1);
             };
-            float M = -INFINITY;
-            for (int cc = c1; cc <= c2; ++cc) {
-              if (!cta_has_units(cc, W, C)) continue;
-              M = fmaxf(M, cc == c ? m_run : __ldcg(slot_base(slot_of(cc)) + D * 128));
-            }
-            float Ls = 0.f;
-            for (int cc = c1; cc <= c2; ++cc) {
-              if (!cta_has_units(cc, W, C)) continue;
-              const float *r = slot_base(slot_of(cc));
-              const float m_p = cc == c ? m_run : __ldcg(r + D * 128);
-              const float l_p = cc == c ? l_run : __ldcg(r + (D + 1) * 128);
-              Ls += (m_p == -INFINITY) ? 0.f : l_p * exp2_approx(m_p - M);
-            }
-            const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+            auto store_chunk = [&](int ch, const float (&acc)[16], float inv) {
+              if (!valid) return;
 #pragma unroll
-            for (int ch = 0; ch < D / 16; ++ch) {
-              float acc[16];
+              for (int q = 0; q < 2; ++q) {
+                uint32_t hw[4];
 #pragma unroll
-              for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+                for (int e = 0; e < 4; ++e) {
+                  __half2 hv = __floats2half2_rn(acc[q * 8 + 2 * e] * inv,
+                                                 acc[q * 8 + 2 * e + 1] * inv);
+                  hw[e] = *reinterpret_cast<uint32_t *>(&hv);
+                }
+                orow[ch * 2 + q] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+              }
+            };
+            constexpr int kFastParts = 3;
+            if (!MASK && W >= C && c2 - c1 < kFastParts) {
+              // Every CTA of [c1, c2] holds a part (W >= C: no CTA is empty), at most
+              // three.  All parts, this CTA's included, are read back from their records,
+              // and every load of a step is issued before any of its values is used: the
+              // (m, l) of all parts in one round trip, then the 16-element chunks with the
+              // next chunk's loads in flight while the current one is folded and stored.
+              const int np = c2 - c1 + 1;
+              const float *rp[kFastParts];
+              float mk[kFastParts], lk[kFastParts], fk[kFastParts];
+#pragma unroll
+              for (int k = 0; k < kFastParts; ++k) {
+                rp[k] = slot_base(slot_of(k < np ? c1 + k : c1));
+                mk[k] = k < np ? __ldcg(rp[k] + D * 128) : -INFINITY;
+                lk[k] = k < np ? __ldcg(rp[k] + (D + 1) * 128) : 0.f;
+              }
+              float M = -INFINITY;
+#pragma unroll
+              for (int k = 0; k < kFastParts; ++k) M = fmaxf(M, mk[k]);
+              float Ls = 0.f;
+#pragma unroll
+              for (int k = 0; k < kFastParts; ++k) {
+                fk[k] = (mk[k] == -INFINITY) ? 0.f : exp2_approx(mk[k] - M);
+                if (k < np) Ls += (mk[k] == -INFINITY) ? 0.f : lk[k] * fk[k];
+              }
+              const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+              float vb[2][kFastParts][16];
+              auto load_chunk = [&](int ch, float (&v)[kFastParts][16]) {
+#pragma unroll
+                for (int k = 0; k < kFastParts; ++k)
+#pragma unroll
+                  for (int e = 0; e < 16; ++e)
+                    v[k][e] = k < np ? __ldcg(rp[k] + (ch * 16 + e) * 128) : 0.f;
+              };
+              load_chunk(0, vb[0]);
+#pragma unroll
+              for (int ch = 0; ch < D / 16; ++ch) {
+                if (ch + 1 < D / 16) load_chunk(ch + 1, vb[(ch + 1) & 1]);
+                float acc[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+#pragma unroll
+                for (int k = 0; k < kFastParts; ++k) {
+                  if (k >= np) continue;
+#pragma unroll
+                  for (int e = 0; e < 16; ++e) acc[e] += fk[k] * vb[ch & 1][k][e];
+                }
+                store_chunk(ch, acc, inv);
+              }
+            } else {
+              // any number of parts: this CTA's own part from registers, the others one
+              // chunk at a time
+              float M = -INFINITY;
               for (int cc = c1; cc <= c2; ++cc) {
                 if (!cta_has_units(cc, W, C)) continue;
-                if (cc == c) {
-                  const float f = (m_run == -INFINITY) ? 0.f : exp2_approx(m_run - M);
-#pragma unroll
-                  for (int e = 0; e < 16; ++e) acc[e] += f * __uint_as_float(o[ch * 16 + e]);
-                } else {
-                  const float *r = slot_base(slot_of(cc));
-                  float v[16];
-                  const float m_p = __ldcg(r + D * 128);
-#pragma unroll
-                  for (int e = 0; e < 16; ++e) v[e] = __ldcg(r + (ch * 16 + e) * 128);
-                  const float f = (m_p == -INFINITY) ? 0.f : exp2_approx(m_p - M);
-#pragma unroll
-                  for (int e = 0; e < 16; ++e) acc[e] += f * v[e];
-                }
+                M = fmaxf(M, cc == c ? m_run : __ldcg(slot_base(slot_of(cc)) + D * 128));
               }
-              if (valid) {
+              float Ls = 0.f;
+              for (int cc = c1; cc <= c2; ++cc) {
+                if (!cta_has_units(cc, W, C)) continue;
+                const float *r = slot_base(slot_of(cc));
+                const float m_p = cc == c ? m_run : __ldcg(r + D * 128);
+                const float l_p = cc == c ? l_run : __ldcg(r + (D + 1) * 128);
+                Ls += (m_p == -INFINITY) ? 0.f : l_p * exp2_approx(m_p - M);
+              }
+              const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
 #pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                  uint32_t hw[4];
+              for (int ch = 0; ch < D / 16; ++ch) {
+                float acc[16];
 #pragma unroll
-                  for (int e = 0; e < 4; ++e) {
-                    __half2 hv = __floats2half2_rn(acc[q * 8 + 2 * e] * inv,
-                                                   acc[q * 8 + 2 * e + 1] * inv);
-                    hw[e] = *reinterpret_cast<uint32_t *>(&hv);
+                for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+                for (int cc = c1; cc <= c2; ++cc) {
+                  if (!cta_has_units(cc, W, C)) continue;
+                  if (cc == c) {
+                    const float f = (m_run == -INFINITY) ? 0.f : exp2_approx(m_run - M);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) acc[e] += f * __uint_as_float(o[ch * 16 + e]);
+                  } else {
+                    const float *r = slot_base(slot_of(cc));
+                    float v[16];
+                    const float m_p = __ldcg(r + D * 128);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) v[e] = __ldcg(r + (ch * 16 + e) * 128);
+                    const float f = (m_p == -INFINITY) ? 0.f : exp2_approx(m_p - M);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) acc[e] += f * v[e];
                   }
-                  orow[ch * 2 + q] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
                 }
+                store_chunk(ch, acc, inv);
               }
             }
             if (lane == 0) *my_cnt = 0;  // ready for the next run of this plan

@@ -313,7 +313,7 @@ def test_forward_fp8_tiny(pa, min_run):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("Hq,Hkv", [(8, 2), (32, 8), (8, 8)])
+@pytest.mark.parametrize("Hq,Hkv", [(8, 2), (32, 8), (8, 8), (16, 8), (64, 8)])
 @pytest.mark.parametrize("min_run", [1, 16], ids=["all_prefill", "default"])
 def test_forward_fp8_small_mixed(pa, Hq, Hkv, min_run):
     from tests._gpu import assert_attn_close
@@ -387,3 +387,32 @@ def test_prefill_fp8_refuses_other_shapes(pa):
         pa.forward_fp8(q, *pool, torch.from_numpy(tpt).to(dev), torch.from_numpy(kv).to(dev),
                        case.scale)
     assert e.value.status == pa.PA_EUNSUPPORTED
+
+
+@pytest.mark.gpu
+def test_prefill_fp8_and_decode_fp8_split_a_mixed_plan(pa):
+    """prefill_fp8 and decode_fp8 on one mixed plan write disjoint tokens: together
+    they give forward_fp8's output bit for bit."""
+    case = workloads.small_prefill(9, P=128, d=128, Hq=32, Hkv=8)
+    ref, pool, tpt, kv = fp8_on_gpu(pa, case)
+    full, err = run_forward_fp8(pa, case, pool, tpt, kv, 16)
+    assert err == 0
+    dev = "cuda"
+    q = torch.from_numpy(case.q.view(np.float16)).to(dev)
+    out = torch.full_like(q, float("nan"))
+    ws = pa.new_workspace(case.T, case.Hq, case.Hkv, 128, dev)
+    tpt_d, kv_d = torch.from_numpy(tpt).to(dev), torch.from_numpy(kv).to(dev)
+    old = pa.set_prefill_min_run(16)
+    try:
+        pa.plan(tpt_d, kv_d, case.Hq, case.Hkv, 128, 128, ws)
+    finally:
+        pa.set_prefill_min_run(old)
+    pa.prefill_fp8(q, *pool, tpt_d, kv_d, case.scale, out, ws)
+    part = out.float().cpu().numpy()
+    pf_rows = ~np.isnan(part).any(axis=(1, 2))
+    assert pf_rows.any() and not pf_rows.all()  # both paths have tokens
+    pa.decode_fp8(q, *pool, tpt_d, kv_d, case.scale, out, ws)
+    torch.cuda.synchronize()
+    assert pa.read_error(ws) == 0
+    both = out.float().cpu().numpy()
+    assert np.array_equal(both, full)
