@@ -193,7 +193,7 @@ __device__ __forceinline__ bool dec_wait(uint64_t *bar, uint32_t parity, int *er
   }
 }
 
-// The consumers' wait for stage k.  Every consumer warp must reach the same verdict,
+// The consumers' wait for stage k.  Every consumer warp must reach the same decision,
 // since they meet at named barriers afterwards: once the CTA gives up, stage k is still
 // consumed if the producer had issued it (its copies land; wait for them), and
 // abandoned only when the producer has stopped short of it.  The last-resort bound,
