@@ -416,3 +416,29 @@ def test_prefill_fp8_and_decode_fp8_split_a_mixed_plan(pa):
     assert pa.read_error(ws) == 0
     both = out.float().cpu().numpy()
     assert np.array_equal(both, full)
+
+
+@pytest.mark.gpu
+def test_forward_fp8_zero_kv_rows_and_empty_ubatch(pa):
+    """kv_len 0 gives zero rows on both paths (a whole prefill tile of them too), and an
+    empty ubatch is a no-op."""
+    from tests._gpu import assert_attn_close
+    case = workloads.small_prefill(10, P=128, d=128, Hq=32, Hkv=8,
+                                   chunks=((0, 300, 181), (1, 0, 130)), extra_decode=3)
+    ref, pool, tpt, kv = fp8_on_gpu(pa, case)
+    kv = kv.copy()
+    zero = np.r_[np.arange(181, 181 + 130), case.T - 1]  # the second run, a decode token
+    kv[zero] = 0
+    want = oracle.paged_attention_fp8(case.q, *ref, tpt, kv, case.scale)
+    assert np.all(want[zero] == 0.0)
+    got, err = run_forward_fp8(pa, case, pool, tpt, kv, 16)
+    assert err == 0
+    assert np.all(got[zero] == 0.0)
+    assert_attn_close(got, want, "fp8 zero kv rows")
+    dev = "cuda"
+    q0 = torch.empty((0, case.Hq, 128), dtype=torch.float16, device=dev)
+    t0 = torch.empty((0, tpt.shape[1]), dtype=torch.int32, device=dev)
+    k0 = torch.empty((0,), dtype=torch.int32, device=dev)
+    out = pa.forward_fp8(q0, *pool, t0, k0, case.scale,
+                         workspace=pa.new_workspace(1, case.Hq, case.Hkv, 128, dev))
+    assert out.shape == (0, case.Hq, 128)
