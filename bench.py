@@ -40,14 +40,14 @@ METRIC = "decode KV GB/s + prefill TFLOP/s, Qwen3-8B-shape paged attn, 8×16K, 1
 # k_decode_fp8_longtail: one FP8 launch of `profile_case fp8` / `fp8_longtail`; k_copy_pages: one launch of `profile_case copy` (writes still
 # in L2 at the end of the launch are not counted).  Summaries and commands: profiles/.
 TRAFFIC = {
-    "k_prefill": {"bytes": 399.25e6, "files": ["k_prefill.cu"], "digest": "81914d0bdbb4fc41"},
-    "k_prefill_fp8": {"bytes": 216.45e6, "files": ["k_prefill.cu"], "digest": "81914d0bdbb4fc41"},
-    "k_decode": {"bytes": 86.31e6, "files": ["k_decode.cu"], "digest": "09be4cb3b3b619e0"},
-    "k_decode_longtail": {"bytes": 1082.34e6, "files": ["k_decode.cu"], "digest": "09be4cb3b3b619e0"},
-    "k_decode_span": {"bytes": 116.64e6, "files": ["k_decode.cu"], "digest": "09be4cb3b3b619e0"},
-    "k_decode_fp8": {"bytes": 43.69e6, "files": ["k_decode.cu"], "digest": "09be4cb3b3b619e0"},
-    "k_decode_fp8_longtail": {"bytes": 559.81e6, "files": ["k_decode.cu"], "digest": "09be4cb3b3b619e0"},
-    "k_copy_pages": {"bytes": 488.04e6, "files": ["k_small.cu"], "digest": "8ffc91b37d609dbd"},
+    "k_prefill": {"bytes": 397.60e6, "files": ["k_prefill.cu"], "digest": "d64645999e60d5cd"},
+    "k_prefill_fp8": {"bytes": 216.40e6, "files": ["k_prefill.cu"], "digest": "d64645999e60d5cd"},
+    "k_decode": {"bytes": 86.21e6, "files": ["k_decode.cu"], "digest": "7c09222e8332d9bc"},
+    "k_decode_longtail": {"bytes": 1081.85e6, "files": ["k_decode.cu"], "digest": "7c09222e8332d9bc"},
+    "k_decode_span": {"bytes": 116.18e6, "files": ["k_decode.cu"], "digest": "7c09222e8332d9bc"},
+    "k_decode_fp8": {"bytes": 43.68e6, "files": ["k_decode.cu"], "digest": "7c09222e8332d9bc"},
+    "k_decode_fp8_longtail": {"bytes": 559.86e6, "files": ["k_decode.cu"], "digest": "7c09222e8332d9bc"},
+    "k_copy_pages": {"bytes": 488.15e6, "files": ["k_small.cu"], "digest": "8ffc91b37d609dbd"},
 }
 _TRAFFIC_HEADERS = ["common.cuh", "tc.cuh", "tmap.cuh", "kernels.cuh"]
 
