@@ -351,11 +351,13 @@ int paged_attn_decode_fp8(const uint16_t *q, const uint8_t *k8_pages, const uint
  * Tensor-core prefill tiles over FP8 pages: the tokens of the workspace's plan's
  * tiles (from paged_attn_plan or paged_attn_plan_prefill for the same tables), as
  * paged_attn_prefill.  Layout, page size, head dimension and scale arrays as
- * paged_attn_decode_fp8.  Each key block's codes are widened in shared memory to
- * binary16(code * scale) -- the value a binary16 cache of the dequantised rows would
- * hold -- and the tile then runs the binary16 MMAs of paged_attn_prefill; V rows past
- * a tile's longest kv_len are cleared, so unwritten cells (NaN codes included) never
- * reach the output.  A scale below the binary16 range (2^-24) widens to zero.
+ * paged_attn_decode_fp8.  Each key block's codes are widened in shared memory: K to
+ * binary16(code * scale), the value a binary16 cache of the dequantised rows would
+ * hold; V to the exact code values, with each key's V scale carried by the
+ * probabilities (binary16(p * scale)), as in paged_attn_decode_fp8.  The tile then runs
+ * the binary16 MMAs of paged_attn_prefill.  Keys past a tile's longest kv_len get
+ * cleared V codes and a zero scale, so unwritten cells (NaN codes included) never
+ * reach the output.  A K scale below the binary16 range (2^-24) widens to zero.
  * PA_ERR_PAGE_RANGE as paged_attn_forward.  One launch.
  */
 int paged_attn_prefill_fp8(const uint16_t *q, const uint8_t *k8_pages, const uint8_t *v8t_pages,
