@@ -89,3 +89,53 @@ def test_prefill_8x16k_schedule_matches_oracle():
         sel, g = got[u]
         ref = oracle.paged_attention(q, kf, vf, tpt, kv, wl.scale, tokens=sel)
         assert_attn_close(g, ref, f"8x16K ubatch {u} ({len(sel)} tokens x {wl.Hq} heads)")
+
+
+def test_prefill_8x16k_schedule_over_fp8_pages_matches_oracle():
+    """The same 65 ubatches over FP8 pages: each through expand -> quantising append ->
+    forward_fp8 (plan + tensor-core prefill over widened codes + split-KV decode).  The
+    final FP8 pool is compared bit for bit with the oracle's quantising append of every
+    row; the checked ubatches' sampled tokens x all heads with the oracle's attention over
+    the dequantised codes."""
+    import paged_kv_cache_pages_gb300 as pa
+    wl = workloads.Prefill8x16K(0)
+    dev = "cuda"
+    spt = torch.from_numpy(wl.seq_page_table).to(dev)
+    nan_codes = lambda shape: np.full(shape, 0x7F, np.uint8)  # noqa: E731
+    N, Hkv, P, d = wl.num_pages, wl.Hkv, wl.P, wl.d
+    host = [nan_codes((N, Hkv, P, d)), nan_codes((N, Hkv, d, P)),
+            np.full((N, Hkv, P), np.nan, np.float32), np.full((N, Hkv, P), np.nan, np.float32)]
+    pool = [torch.from_numpy(x).to(dev) for x in host]
+    Tmax = max(ts.shape[0] for ts, _ in wl.ubatches)
+    ws = pa.new_workspace(Tmax, wl.Hq, Hkv, d, dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    got = {}
+    for u in range(len(wl.ubatches)):
+        ts, tp, q, k, v = wl.ubatch(u)
+        f16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.float16)).to(dev)  # noqa
+        tpt, kv, slot = pa.expand_ubatch(spt, torch.from_numpy(ts).to(dev),
+                                         torch.from_numpy(tp).to(dev), P, err=err)
+        pa.kv_append_fp8(f16(k), f16(v), slot, *pool, err=err)
+        out = pa.forward_fp8(f16(q), *pool, tpt, kv, wl.scale, workspace=ws)
+        if u in CHECK:
+            sel = sample_tokens(ts)
+            got[u] = (sel, out[torch.from_numpy(sel).long().to(dev)].float().cpu().numpy())
+            assert pa.read_error(ws) == 0, f"device error word set in ubatch {u}"
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+
+    # the oracle's quantising append of every row of the 8 sequences
+    K, V = wl._draw_kv()
+    pos = np.arange(wl.seq_len)
+    slots = np.concatenate([wl.seq_page_table[s][pos // P].astype(np.int64) * P + pos % P
+                            for s in range(wl.n_seq)])
+    oracle.kv_append_fp8(K.reshape(-1, Hkv, d), V.reshape(-1, Hkv, d), slots, *host)
+    for g_, h_ in zip(pool, host):
+        assert np.array_equal(g_.cpu().numpy().view(np.uint8), h_.view(np.uint8))
+
+    for u in CHECK:
+        ts, tp, q, _, _ = wl.ubatch(u)
+        tpt, kv, _ = oracle.expand_ubatch(wl.seq_page_table, ts, tp, P)
+        sel, g = got[u]
+        ref = oracle.paged_attention_fp8(q, *host, tpt, kv, wl.scale, tokens=sel)
+        assert_attn_close(g, ref, f"8x16K FP8 ubatch {u} ({len(sel)} tokens x {wl.Hq} heads)")
