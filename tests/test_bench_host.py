@@ -60,3 +60,15 @@ def test_decode_cpu_baseline_counts_the_layer_bytes():
     r = bench.cpu_baseline_decode(case, reps_budget_s=0.05)
     assert r["kind"] == "oracle" and r["unit"] == "GB/s" and r["value"] > 0
     assert r["cores"] >= 1 and "runs in" in r["sample"]
+
+
+def test_every_traffic_key_the_bench_asks_for_has_a_record():
+    """Each `traffic_of(...)` key that bench.py reads names a record (a missing key would
+    silently report null traffic)."""
+    import re
+    with open(bench.__file__) as fh:
+        src = fh.read()
+    keys = set(re.findall(r'traffic_of\("([a-z0-9_]+)"\)', src))
+    keys |= set(re.findall(r'traffic_key="([a-z0-9_]+)"', src))
+    assert keys, "no traffic keys found"
+    assert keys <= set(bench.TRAFFIC), sorted(keys - set(bench.TRAFFIC))
